@@ -1,0 +1,164 @@
+/*
+ * attn.h - C ABI of libattn.so: causal scaled dot-product attention with RoPE
+ * and GQA/MQA head sharing on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is
+ *     O = softmax(Q' K'^T * scale + M) V,   Q' = RoPE(Q), K' = RoPE(K)
+ * per head, with M[m, n] = -inf for keys after the query
+ * ("Transformer架构从Attention到DecoderBlock" §4.2-§4.5, eq. head_i; the mask of
+ * "2.7 Transformer Decoder Block完整解析" §3.2), RoPE rotating each dimension pair
+ * (2i, 2i+1) by pos * base^(-2i/D) ("Transformer架构从Attention到DecoderBlock"
+ * §8.2-§8.3) and query head h reading KV head floor(h / (n_h / n_kv)) (§6.3).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    keeps no pointer after a call returns and allocates no device memory.
+ *  - Tensors are dense, row-major, innermost dimension last; activations use the
+ *    BSHD layout [batch, sequence, heads, head_dim].
+ *  - dtype selects the element type of q/k/v/out/caches: ATTN_F32 (float) or
+ *    ATTN_BF16 (__nv_bfloat16).  Arithmetic is fp32 in either case; bf16 inputs
+ *    feed bf16 tensor-core MMAs with fp32 accumulation.
+ *  - stream is a cudaStream_t passed as void*; NULL is the legacy default stream.
+ *    Calls only enqueue work: they return before the kernels finish.
+ *  - Return value: ATTN_OK (0) or a negative ATTN_ERR_* code.  Argument errors
+ *    are detected on the host before anything is launched.  A device-side
+ *    bounded wait that expires is reported later by attn_device_status().
+ *  - All pointers must be 16-byte aligned (vector and TMA loads), else
+ *    ATTN_ERR_ALIGN.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_ARG = -1,          /* null pointer, non-positive size, n_h % n_kv != 0, bad span */
+  ATTN_ERR_UNSUPPORTED = -2,  /* a head dim / dtype combination no kernel handles */
+  ATTN_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned */
+  ATTN_ERR_CUDA = -4,         /* the CUDA runtime rejected a launch (no device, bad stream...) */
+  ATTN_ERR_TIMEOUT = -5,      /* a bounded device wait expired (reported by attn_device_status) */
+  ATTN_ERR_WORKSPACE = -6     /* the caller's workspace is smaller than required */
+};
+
+/* Static, human-readable text for a return code. Never NULL. */
+ATTN_API const char* attn_strerror(int code);
+
+/*
+ * attn_prefill - attention over whole prompts (prefill), never materialising S.
+ *
+ * Defined by "Transformer架构从Attention到DecoderBlock" §4.5 (head_i = softmax(
+ * Q_i K_i^T / sqrt(D_h) + M) V_i) with §13.1 (prefill: the whole prompt at once);
+ * computed tile by tile with the online softmax of "Transformer架构完全深度解析"
+ * §13 (running max m and sum l), skipping key tiles that lie wholly after the
+ * query tile ("2.7 Transformer Decoder Block完整解析" §3.3).
+ *
+ *   q      [B, S, n_h,  D_h]  queries, NOT rotated.
+ *   k      [B, S, n_kv, D_h]  keys, NOT rotated.
+ *   v      [B, S, n_kv, D_h]  values (never rotated).
+ *   out    [B, S, n_h,  D_h]  result, same dtype.
+ *   k_rot  [B, S, n_kv, D_h]  receives RoPE(K), the rotated keys a KV cache
+ *                             stores ("Transformer架构完全深度解析" §7).  Required
+ *                             when rope_base > 0, ignored (may be NULL) otherwise.
+ *                             It must not overlap k.
+ *   lse    [B, n_h, S] fp32   optional (NULL to skip): natural-log normaliser
+ *                             log sum_n exp(score[m, n]) of each query row.
+ *   rope_base  > 0: rotate Q and K with theta_i = rope_base^(-2i/D_h); <= 0: no RoPE.
+ *   scale      > 0: score multiplier; <= 0: 1/sqrt(D_h).
+ *   causal     1: mask keys n > m (the diagonal stays visible); 0: no mask.
+ * Supported: ATTN_F32 with D_h even, 2 <= D_h <= 256; ATTN_BF16 with D_h a
+ * multiple of 8, 8 <= D_h <= 256.  n_h must be a multiple of n_kv.
+ */
+ATTN_API int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k_rot,
+                 float* lse, int B, int S, int n_h, int n_kv, int D_h, float rope_base,
+                 float scale, int causal, attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_rope - rotate dims [rope_offset, rope_offset + rope_dims) of every row
+ * of x_in [B, S, n_heads, D] at position pos_offset + s (s = sequence index),
+ * pairing (2i, 2i+1) with theta_i = rope_base^(-2i/rope_dims)
+ * ("Transformer架构从Attention到DecoderBlock" §8.2-§8.3).  Dims outside the span
+ * are copied unchanged.  x_out may equal x_in (in place) but must not partially
+ * overlap it.  rope_offset, rope_dims and D must be multiples of 8 (bf16) or
+ * 2 (f32); rope_base must be > 0.  This is the step that fills a cache with
+ * rotated keys.
+ */
+ATTN_API int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D,
+              int rope_offset, int rope_dims, float rope_base, int pos_offset,
+              attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_decode_workspace_size - bytes of device scratch attn_decode needs for
+ * these sizes (0 is never returned for valid sizes; -1 cast to size_t for
+ * invalid ones).  The caller allocates it; it may be reused across calls that
+ * do not overlap on the GPU.
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len,
+                                  attn_dtype_t dtype);
+
+/*
+ * attn_decode - one new query token per sequence against its KV cache.
+ *
+ * Defined by "Transformer架构完全深度解析" §9 (K_cache = concat(K_cache, K_new),
+ * then Attention(Q[t+1], K_cache, V_cache)) and "Transformer架构从Attention到
+ * DecoderBlock" §13.2.  The cache holds rotated keys, so only q is rotated, at
+ * position seqlens[b] - 1.  The key range is split into chunks processed in
+ * parallel; their partial results are merged with the running-max /
+ * running-sum rule of the online softmax ("Transformer架构完全深度解析" §13).
+ * With n_kv = 1, D_qk = 576, D_v = 512 and vcache aliasing kcache this is the
+ * MLA-absorbed decode of "Transformer 与 LLM" slide 06 (128 heads sharing one
+ * 576-dim latent head; pass scale = 1/sqrt(192)).
+ *
+ *   q        [B, n_h, D_qk]          new queries, NOT rotated.
+ *   kcache   [B, max_len, n_kv, D_qk] rotated keys; rows >= seqlens[b] are never read.
+ *   vcache   values: element (b, t, g, d) at vcache[(b*max_len + t)*v_token_stride + g*D_v + d].
+ *   v_token_stride  elements between consecutive tokens of vcache; 0 means n_kv*D_v.
+ *                   MLA passes vcache = kcache and v_token_stride = D_qk.
+ *   seqlens  DEVICE int32 [B]: valid keys per sequence INCLUDING the new token,
+ *            1 <= seqlens[b] <= max_len (out-of-range values are clamped on the device).
+ *   out      [B, n_h, D_v]  result, same dtype.
+ *   lse      optional fp32 [B, n_h] natural-log normaliser (NULL to skip).
+ *   rope_base > 0 rotates q dims [rope_offset, rope_offset + rope_dims); <= 0: no RoPE.
+ *   scale     > 0: score multiplier; <= 0: 1/sqrt(D_qk).
+ *   workspace device scratch of at least attn_decode_workspace_size(...) bytes,
+ *             16-byte aligned, owned by the caller; its contents on entry are ignored.
+ * Supported: D_qk, D_v multiples of 8 up to 576 and 512; n_h / n_kv <= 128.
+ */
+ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, int v_token_stride,
+                const int* seqlens, void* out, float* lse, int B, int n_h, int n_kv, int D_qk,
+                int D_v, int max_len, float rope_base, int rope_offset, int rope_dims,
+                float scale, attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
+ * attn_device_status - synchronise the stream, then return ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if a kernel of this library gave up on a bounded wait since
+ * the last call (the flag is cleared), or ATTN_ERR_CUDA if the stream reports
+ * an error.
+ */
+ATTN_API int attn_device_status(void* stream);
+
+/* Number of kernels this library has launched since it was loaded. */
+ATTN_API unsigned long long attn_launch_count(void);
+
+/* Set the per-wait limit of device-side bounded waits, in nanoseconds
+ * (default 2e9).  Applies to launches made after the call. */
+ATTN_API void attn_set_wait_limit_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -259,10 +259,10 @@ def attention_decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0,
         for g in range(n_kv):
             kk = _f64(kcache[b, :L, g, :])
             vv = _f64(vcache[b, :L, g, :])
-            for h in range(g * G, (g + 1) * G):
-                o, _, l = attention_head(qb[h:h + 1], kk, vv, scale, mask)
-                out[b, h] = o[0]
-                lse[b, h] = l[0]
+            # the G query heads of this KV head share K and V; each is one row
+            o, _, l = attention_head(qb[g * G:(g + 1) * G], kk, vv, scale, mask)
+            out[b, g * G:(g + 1) * G] = o
+            lse[b, g * G:(g + 1) * G] = l
     return out, lse
 
 

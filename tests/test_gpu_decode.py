@@ -1,0 +1,103 @@
+"""Decode parity: split-KV decode (through the C ABI) against the fp64 oracle.
+
+Covers the GQA decode configuration (59 sequences, 4096..8192 cached keys) and
+the MLA-absorbed configuration (32 x 32768 keys, one 576-dim latent head, V =
+its first 512 dims) in full, small cases with ragged lengths down to a single
+key, fp32, RoPE on part of the latent, and the pages' statement that decoding
+with a cache reproduces the full prefill token by token.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.tolerances import BF16_MAX_ABS, assert_parity, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_causal_attention_gb300 as attn
+    yield attn
+    assert attn.device_status() == 0
+
+
+def run_decode(attn, cfg, q, kc, vc, sl):
+    kc_d = kc.to(DEV)
+    vc_d = kc_d[..., :cfg["D_v"]] if cfg.get("v_aliases_k") else vc.to(DEV)
+    out, lse = attn.decode(q.to(DEV), kc_d, vc_d, sl.to(DEV), rope_base=cfg["rope_base"],
+                           rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
+                           lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_decode(cfg, q, kc, vc, sl, batch_index=None):
+    return oracle.attention_decode(q, kc, vc, sl.numpy(), rope_base=cfg["rope_base"],
+                                   rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"],
+                                   scale=cfg["scale"], batch_index=batch_index)
+
+
+SMALL = [
+    # B, n_h, n_kv, D_qk, D_v, max_len, rope_base, rope_offset, rope_dims, alias, dtype
+    (4, 32, 8, 128, 128, 700, 5e5, 0, 128, False, "bf16"),
+    (3, 8, 8, 64, 64, 300, 1e4, 0, 64, False, "bf16"),
+    (2, 6, 3, 128, 64, 1030, 0.0, 0, 128, False, "bf16"),
+    (2, 16, 1, 576, 512, 300, 0.0, 512, 64, True, "bf16"),
+    (2, 16, 1, 576, 512, 300, 1e4, 512, 64, True, "bf16"),
+    (3, 4, 2, 64, 64, 100, 1e4, 0, 64, False, "f32"),
+]
+
+
+@pytest.mark.parametrize("B,n_h,n_kv,Dqk,Dv,L,rope,roff,rdims,alias,dtype", SMALL)
+def test_decode_small(lib, B, n_h, n_kv, Dqk, Dv, L, rope, roff, rdims, alias, dtype):
+    cfg = dict(B=B, n_h=n_h, n_kv=n_kv, D_qk=Dqk, D_v=Dv, max_len=L, len_lo=1, len_hi=L,
+               v_aliases_k=alias, dtype=dtype, rope_base=rope, rope_offset=roff, rope_dims=rdims,
+               scale=1 / math.sqrt(192) if alias else 0.0)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=L)
+    sl[0] = 1           # a sequence holding only its new token
+    sl[-1] = L          # and one filling the cache
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, dtype, f"decode {cfg}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= (1e-4 if dtype == "f32" else BF16_MAX_ABS)
+
+
+def test_gqa_decode_config_full(lib):
+    cfg = workloads.config("gqa_decode")
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=0)
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", "gqa decode")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+def test_mla_decode_config_full(lib):
+    cfg = workloads.config("mla_decode")
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=0)
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", "mla decode")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+def test_decode_with_cache_matches_prefill_token_by_token(lib):
+    # "Transformer 与 LLM" slide 02: outputs with and without the KV cache agree token by token
+    B, S, n_h, n_kv, D, base = 2, 300, 8, 2, 128, 5e5
+    cfg = dict(B=B, S=S, n_h=n_h, n_kv=n_kv, D_h=D, dtype="bf16")
+    q, k, v = workloads.prefill_inputs(cfg, seed=11)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    full, krot, _ = lib.prefill(qd, kd, vd, rope_base=base)          # krot is the rotated-K cache
+    for t in (0, 1, 127, 128, 299):
+        sl = torch.full((B,), t + 1, dtype=torch.int32, device=DEV)
+        out, _ = lib.decode(qd[:, t].contiguous(), krot, vd, sl, rope_base=base)
+        ref = oracle.attention_prefill(q, k, v, rope_base=base)[:, t]
+        assert_parity(out, ref, "bf16", f"decode t={t}")
+        assert_parity(out, to_np(full[:, t]), "bf16", f"decode vs prefill t={t}")

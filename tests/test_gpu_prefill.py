@@ -1,0 +1,140 @@
+"""Prefill parity: the CUDA library (through the C ABI) against the fp64 oracle.
+
+Covers the tiny fp32 configuration, the GPT-2-shaped configuration in full,
+the Llama-3-8B-shaped configuration at full size on sampled rows (in the launch
+configuration the benchmark times), and small cases that span several tiles,
+a ragged tail, S = 1, MQA, non-causal masking, the CUDA-core path for other
+head sizes, the online-softmax rescale branch and causality.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.tolerances import BF16_MAX_ABS, assert_parity, errors, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_causal_attention_gb300 as attn
+    yield attn
+    assert attn.device_status() == 0
+
+
+def gpu_prefill(attn, cfg, q, k, v):
+    out, krot, lse = attn.prefill(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
+                                  scale=cfg["scale"], causal=cfg.get("causal", True), lse=True)
+    torch.cuda.synchronize()
+    return out, krot, lse
+
+
+def test_tiny_config(lib):
+    cfg = workloads.config("tiny")
+    q, k, v = workloads.prefill_inputs(cfg, seed=0)
+    out, krot, lse = gpu_prefill(lib, cfg, q, k, v)
+    ref, ref_lse = oracle.attention_prefill(q, k, v, rope_base=cfg["rope_base"], scale=cfg["scale"],
+                                            return_lse=True)
+    assert_parity(out, ref, "f32", "tiny out")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= 1e-4
+    assert np.max(np.abs(to_np(krot) - oracle.rope_cache(k, cfg["rope_base"]))) <= 1e-5
+
+
+CASES = [
+    # B, S, n_h, n_kv, D, rope_base, causal
+    (1, 300, 4, 2, 128, 5e5, True),    # tensor cores, GQA, ragged tail (3 tiles)
+    (2, 256, 2, 2, 64, 0.0, True),     # tensor cores D=64, exact tile pair
+    (1, 77, 4, 1, 128, 1e4, True),     # MQA, one partial tile
+    (1, 1, 2, 1, 64, 1e4, True),       # a single token
+    (1, 200, 2, 2, 128, 1e4, False),   # no mask, ragged key tile
+    (1, 520, 8, 2, 64, 1e4, True),     # five tiles: an odd last pair
+    (2, 1024, 4, 4, 128, 1e4, True),   # eight tiles per head
+    (1, 130, 2, 2, 96, 1e4, True),     # CUDA-core path (D_h 96)
+    (1, 64, 2, 1, 256, 1e4, True),     # CUDA-core path (D_h 256)
+]
+
+
+@pytest.mark.parametrize("B,S,n_h,n_kv,D,rope,causal", CASES)
+def test_bf16_prefill_cases(lib, B, S, n_h, n_kv, D, rope, causal):
+    cfg = dict(B=B, S=S, n_h=n_h, n_kv=n_kv, D_h=D, dtype="bf16", rope_base=rope, scale=0.0, causal=causal)
+    q, k, v = workloads.prefill_inputs(cfg, seed=S + D)
+    out, krot, lse = gpu_prefill(lib, cfg, q, k, v)
+    ref, ref_lse = oracle.attention_prefill(q, k, v, rope_base=rope, causal=causal, return_lse=True)
+    assert_parity(out, ref, "bf16", f"out {cfg}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+    if rope > 0:
+        assert_parity(krot, oracle.rope_cache(k, rope), "bf16", "k_rot")
+
+
+def test_gpt2_config_full(lib):
+    cfg = workloads.config("gpt2")
+    q, k, v = workloads.prefill_inputs(cfg, seed=0)
+    out, _, lse = gpu_prefill(lib, cfg, q, k, v)
+    ref, ref_lse = oracle.attention_prefill(q, k, v, rope_base=0.0, scale=cfg["scale"], return_lse=True)
+    assert_parity(out, ref, "bf16", "gpt2")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+def test_llama_config_sampled_rows(lib):
+    cfg = workloads.config("llama3_8b")
+    q, k, v = workloads.prefill_inputs(cfg, seed=0)
+    out, krot, lse = gpu_prefill(lib, cfg, q, k, v)
+    out_c, krot_c, lse_c = out.cpu(), krot.cpu(), lse.cpu()
+    rows = [0, 1, 127, 128, 255, 256, 4095, 4096, 8063, 8064, 8190, 8191]
+    rng = np.random.default_rng(0)
+    got, want = [], []
+    for b, h in [(0, 0), (3, 31), (1, 17), (2, 6)]:
+        sel = sorted(set(rows) | set(rng.integers(0, cfg["S"], 6).tolist()))
+        ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, sel, rope_base=cfg["rope_base"],
+                                                     scale=cfg["scale"])
+        got.append(to_np(out_c[b, sel, h]))
+        want.append(ref)
+        assert np.max(np.abs(to_np(lse_c[b, h, sel]) - ref_lse)) <= BF16_MAX_ABS
+    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", "llama sampled rows")
+    # rotated keys (the cache the prefill writes) on sampled rows of every KV head
+    sel = [0, 1, 4095, 8191]
+    ref_k = oracle.rope_rotate(k[2, sel], np.array(sel)[:, None], cfg["rope_base"])
+    assert_parity(krot_c[2, sel], ref_k, "bf16", "llama k_rot")
+
+
+def test_online_softmax_rescale_branch(lib):
+    # scores grow by ~17 (log2 units) from one key tile to the next, so the
+    # running maximum moves past the lazy-rescale threshold on every tile
+    S, D = 640, 64
+    q = torch.zeros(1, S, 1, D)
+    k = torch.zeros(1, S, 1, D)
+    q[..., 0] = 4.0
+    k[0, :, 0, 0] = 3.0 * (torch.arange(S) // 128).float()
+    v = torch.randn(1, S, 1, D, generator=torch.Generator().manual_seed(5))
+    q, k, v = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    cfg = dict(rope_base=0.0, scale=1.0)
+    out, _, _ = gpu_prefill(lib, cfg, q, k, v)
+    ref = oracle.attention_prefill(q, k, v, scale=1.0)
+    assert_parity(out, ref, "bf16", "rescale")
+
+
+def test_causality_future_perturbation_leaves_past_bit_identical(lib):
+    cfg = dict(B=1, S=384, n_h=4, n_kv=2, D_h=128, dtype="bf16", rope_base=1e4, scale=0.0)
+    q, k, v = workloads.prefill_inputs(cfg, seed=9)
+    out, _, _ = gpu_prefill(lib, cfg, q, k, v)
+    m = 200
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    q2[:, m + 1:] = -q2[:, m + 1:]
+    k2[:, m + 1:] += 1.0
+    v2[:, m + 1:] *= 3.0
+    out2, _, _ = gpu_prefill(lib, cfg, q2, k2, v2)
+    assert torch.equal(out[:, :m + 1], out2[:, :m + 1])
+    assert not torch.equal(out[:, m + 1:], out2[:, m + 1:])
+
+
+def test_outputs_are_deterministic(lib):
+    cfg = dict(B=1, S=512, n_h=4, n_kv=1, D_h=128, dtype="bf16", rope_base=5e5, scale=0.0)
+    q, k, v = workloads.prefill_inputs(cfg, seed=3)
+    a, _, _ = gpu_prefill(lib, cfg, q, k, v)
+    b, _, _ = gpu_prefill(lib, cfg, q, k, v)
+    assert torch.equal(a, b)

@@ -1,0 +1,209 @@
+"""ctypes binding of libattn.so: argument marshalling only.
+
+Every function here checks the torch tensors it is given (device, dtype,
+contiguity, shape), allocates outputs with torch when the caller does not pass
+them, and forwards raw device pointers to the C ABI declared in
+include/attn.h.  All arithmetic runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback - a missing library or GPU raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_F32, ATTN_BF16 = 0, 1
+ERRORS = {
+    0: "ATTN_OK", -1: "ATTN_ERR_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_ALIGN",
+    -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_TIMEOUT", -6: "ATTN_ERR_WORKSPACE",
+}
+
+# (name, restype, argtypes) of every exported symbol, mirroring include/attn.h
+_vp, _i, _f, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
+SIGNATURES = [
+    ("attn_strerror", ctypes.c_char_p, [_i]),
+    ("attn_prefill", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
+    ("attn_rope", _i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    ("attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i, _i, _i]),
+    ("attn_decode", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
+                         _vp, _sz, _vp]),
+    ("attn_device_status", _i, [_vp]),
+    ("attn_launch_count", _u64, []),
+    ("attn_set_wait_limit_ns", None, [_u64]),
+]
+
+
+class AttnError(RuntimeError):
+    """A non-zero return code of the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib().attn_strerror(code).decode() if _LIB is not None else ERRORS.get(code, "?")
+        super().__init__(f"{where}: {ERRORS.get(code, code)} ({msg})")
+
+
+_LIB = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "transformer_causal_attention_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libattn.so (raises if it has not been built)."""
+    return _lib()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise AttnError(rc, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _dev(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def prefill(q, k, v, *, rope_base: float = 0.0, scale: float = 0.0, causal: bool = True,
+            out=None, k_rot=None, lse: bool | torch.Tensor = False, stream=None):
+    """Causal (or full) attention over whole prompts via attn_prefill.
+
+    q [B,S,n_h,D], k/v [B,S,n_kv,D] CUDA tensors (bf16 or fp32, contiguous, BSHD).
+    Returns out [B,S,n_h,D]; with rope_base > 0 also returns the rotated keys
+    k_rot [B,S,n_kv,D] (the KV-cache form), and with lse=True the fp32
+    log-sum-exp [B,n_h,S].  Result tuple: (out, k_rot or None, lse or None).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share a dtype")
+    B, S, n_h, D = q.shape
+    n_kv = k.shape[2]
+    if k.shape != (B, S, n_kv, D) or v.shape != (B, S, n_kv, D):
+        raise ValueError("k and v must be [B, S, n_kv, D] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    if rope_base > 0 and k_rot is None:
+        k_rot = torch.empty_like(k)
+    if isinstance(lse, torch.Tensor):
+        lse_t = lse
+    elif lse:
+        lse_t = torch.empty((B, n_h, S), dtype=torch.float32, device=q.device)
+    else:
+        lse_t = None
+    rc = _lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(k_rot) if rope_base > 0 else None,
+                             _ptr(lse_t), B, S, n_h, n_kv, D, float(rope_base), float(scale),
+                             1 if causal else 0, _dtype_code(q), _stream_ptr(stream))
+    _check(rc, "attn_prefill")
+    return out, (k_rot if rope_base > 0 else None), lse_t
+
+
+def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = None, pos_offset: int = 0,
+         out=None, stream=None):
+    """RoPE of x [B,S,n_heads,D] at positions pos_offset + s via attn_rope (out may be x)."""
+    _dev(x, "x")
+    B, S, H, D = x.shape
+    rope_dims = D - rope_offset if rope_dims is None else rope_dims
+    if out is None:
+        out = torch.empty_like(x)
+    rc = _lib().attn_rope(_ptr(out), _ptr(x), B, S, H, D, rope_offset, rope_dims, float(rope_base), pos_offset,
+                          _dtype_code(x), _stream_ptr(stream))
+    _check(rc, "attn_rope")
+    return out
+
+
+def decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len, dtype=torch.bfloat16) -> int:
+    n = _lib().attn_decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len,
+                                          ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F32)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid decode sizes")
+    return n
+
+
+def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: int = 0,
+           rope_dims: int | None = None, scale: float = 0.0, out=None, lse: bool = False, workspace=None,
+           stream=None):
+    """One new token per sequence against its KV cache via attn_decode.
+
+    q [B,n_h,D_qk] (un-rotated), kcache [B,L,n_kv,D_qk] (rotated keys), vcache
+    [B,L,n_kv,D_v] contiguous or a last-dim slice of kcache (MLA: V = the first
+    D_v latent dims), seqlens int32 [B] on the device (keys incl. the new one).
+    Returns (out [B,n_h,D_v], lse [B,n_h] or None).
+    """
+    _dev(q, "q")
+    _dev(kcache, "kcache")
+    if not vcache.is_cuda:
+        raise ValueError("vcache must be a CUDA tensor")
+    if not seqlens.is_cuda or seqlens.dtype != torch.int32:
+        raise ValueError("seqlens must be an int32 CUDA tensor")
+    B, n_h, D_qk = q.shape
+    _, L, n_kv, _ = kcache.shape
+    D_v = vcache.shape[-1]
+    if vcache.is_contiguous():
+        ldv = 0
+    elif vcache.data_ptr() == kcache.data_ptr() and vcache.stride(-1) == 1 and vcache.stride(2) == D_qk:
+        ldv = vcache.stride(1)
+    else:
+        raise ValueError("vcache must be contiguous or a leading slice of kcache's last dim")
+    rope_dims = (D_qk - rope_offset) if rope_dims is None else rope_dims
+    if out is None:
+        out = torch.empty((B, n_h, D_v), dtype=q.dtype, device=q.device)
+    lse_t = torch.empty((B, n_h), dtype=torch.float32, device=q.device) if lse else None
+    need = decode_workspace_size(B, n_h, n_kv, D_qk, D_v, L, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = _lib().attn_decode(_ptr(q), _ptr(kcache), vcache.data_ptr(), ldv, _ptr(seqlens), _ptr(out), _ptr(lse_t),
+                            B, n_h, n_kv, D_qk, D_v, L, float(rope_base), rope_offset, rope_dims, float(scale),
+                            _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream_ptr(stream))
+    _check(rc, "attn_decode")
+    return out, lse_t
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status code."""
+    return _lib().attn_device_status(_stream_ptr(stream))
+
+
+def launch_count() -> int:
+    return int(_lib().attn_launch_count())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib().attn_set_wait_limit_ns(int(ns))

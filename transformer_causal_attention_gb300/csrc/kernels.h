@@ -1,0 +1,62 @@
+// kernels.h - launch interface between the C ABI (api.cu) and the kernel
+// translation units.  Host-side only; nothing here is exported.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;  // keys as the kernels read them: already rotated when RoPE is on
+  const void* v;
+  void* out;
+  float* lse;  // nullable
+  int B, S, n_h, n_kv, D;
+  float scale_log2;  // score multiplier times log2(e)
+  int causal;
+  unsigned int* status;
+  unsigned long long wait_limit_ns;
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* kcache;
+  const void* vcache;
+  long long v_token_stride;  // elements
+  const int* seqlens;
+  void* out;
+  float* lse;  // nullable
+  int B, n_h, n_kv, D_qk, D_v, max_len;
+  int rope_offset;
+  float scale_log2;
+  float* ws_o;    // [B, n_h, n_split, D_v] partial outputs (normalised)
+  float* ws_lse;  // [B, n_h, n_split] partial log2-normalisers
+  int n_split, chunk;
+  unsigned int* status;
+  unsigned long long wait_limit_ns;
+};
+
+struct RopeArgs {
+  void* out;
+  const void* in;
+  int B, S, n_heads, D, rope_offset, rope_dims, pos_offset;
+};
+
+// Each launcher returns the launch error (cudaSuccess when enqueued) and adds
+// the number of kernels it enqueued to *launches.
+cudaError_t launch_prefill_simt(const PrefillArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
+                                int* launches);
+bool prefill_tc_supported(int D, bool bf16);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps,
+                              int num_sms, cudaStream_t st, int* launches);
+cudaError_t launch_rope(const RopeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches);
+int decode_plan_splits(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, int* chunk);
+cudaError_t launch_decode(const DecodeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
+                          int* launches);
+
+}  // namespace attn
