@@ -1,0 +1,422 @@
+"""Throughput of the attention hot path on GB300 (one JSON line on rank 0).
+
+A step is one pass over every kernel of the path on synthetic inputs resident
+in HBM:
+  * prefill - Llama-3-8B-shaped causal GQA prefill, B=4 S=8192 n_h=32 n_kv=8
+    D_h=128 bf16, RoPE base 5e5 (attn_prefill: the RoPE pass writing rotated
+    keys, then the tensor-core attention kernel);
+  * gqa     - GQA decode, 59 sequences with 4096..8192 cached keys, n_h=32
+    n_kv=8 D_h=128 bf16 (attn_decode: split-KV partials + combine);
+  * mla     - MLA-absorbed decode, 32 sequences x 32768 keys, 128 heads over
+    one 576-dim latent head, V = its first 512 dims (attn_decode).
+``value`` is the prefill throughput in TFLOP/s (causal FLOPs = half the dense
+4*B*n_h*S^2*D_h); the decode calls report KV GB/s (algorithmic cache bytes) in
+``parts``.  Every input is larger than the 129 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (each
+step: a block of 256 query rows of one (batch, head) slice of the prefill
+workload, all their visible keys).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "prefill causal-attn TFLOP/s and decode KV GB/s on 1 GB300, % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+# DRAM bytes (read + write) per launch of the prefill kernel, from the ncu
+# capture summarised in profiles/prefill_tc_llama3_8b.md, valid only for the
+# kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits).
+PREFILL_TRAFFIC = {"kernel_sha": None, "bytes": None}
+
+
+def kernel_sha(name: str) -> str:
+    path = os.path.join(ROOT, "transformer_causal_attention_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU) baseline
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_prefill_rows(q, k, v, cfg, b, h, rows):
+    """The oracle on a block of query rows of one (batch, head) slice of the
+    prefill workload; returns (seconds, causal FLOPs of those rows: 4*D_h per
+    visible key, i.e. 2*D_h for q.k and 2*D_h for the weighted value)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attention_prefill_rows(q, k, v, b, h, rows, rope_base=cfg["rope_base"], scale=cfg["scale"])
+    dt = time.perf_counter() - t0
+    return dt, float(sum(4.0 * cfg["D_h"] * (m + 1) for m in rows))
+
+
+def sample_rows(cfg, i, n_rows=256):
+    """The i-th sample: n_rows consecutive query rows of (b, h), spread over the sequence."""
+    b, h = i % cfg["B"], (7 * i) % cfg["n_h"]
+    n_blocks = cfg["S"] // n_rows
+    r0 = ((5 * i + 3) % n_blocks) * n_rows
+    return b, h, list(range(r0, r0 + n_rows))
+
+
+def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 12.0, max_samples: int = 64):
+    done, secs, flops = 0, 0.0, 0.0
+    while done < max_samples and (done == 0 or secs < budget_s):
+        b, h, rows = sample_rows(cfg, done)
+        dt, fl = oracle_prefill_rows(q, k, v, cfg, b, h, rows)
+        secs += dt
+        flops += fl
+        done += 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{done} blocks of 256 query rows from different (batch, head) slices of the prefill "
+                      f"workload (all visible keys each), fp64, {secs:.1f} s"}
+
+
+def cpu_baseline_decode(q, kc, vc, sl, cfg, n_seq: int):
+    import numpy as np
+    import oracle
+    idx = list(range(n_seq))
+    t0 = time.perf_counter()
+    oracle.attention_decode(q, kc, vc, sl.numpy(), rope_base=cfg["rope_base"], rope_offset=cfg["rope_offset"],
+                            rope_dims=cfg["rope_dims"], scale=cfg["scale"], batch_index=idx)
+    dt = time.perf_counter() - t0
+    by = workloads.decode_bytes(cfg, sl[:n_seq].tolist())
+    return {"value": by / dt / 1e9, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{n_seq} of {cfg['B']} sequences, fp64, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = workloads.config("llama3_8b")
+    q, k, v = workloads.prefill_inputs(cfg, seed=0)
+    for i in range(args.warmup):
+        b, h, rows = sample_rows(cfg, i)
+        oracle_prefill_rows(q, k, v, cfg, b, h, rows)
+    secs, flops = 0.0, 0.0
+    for i in range(args.steps):
+        b, h, rows = sample_rows(cfg, args.warmup + i)
+        dt, fl = oracle_prefill_rows(q, k, v, cfg, b, h, rows)
+        secs += dt
+        flops += fl
+    value = flops / secs / 1e12
+    sample = "each step: 256 consecutive query rows of one (batch, head) slice of the prefill workload, fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
+                               " (oracle: 256 query rows of one (b,h) slice per step)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_causal_attention_gb300 as attn
+    lib = attn.load()
+
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs (seeded, CPU-drawn, then resident in HBM)
+    pc = workloads.config("llama3_8b", B=args.prefill_batch)
+    q_h, k_h, v_h = workloads.prefill_inputs(pc, seed=rank)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    out = torch.empty_like(q)
+    k_rot = torch.empty_like(k)
+    gc = workloads.config("gqa_decode")
+    if "gqa" not in args.parts:
+        gc = workloads.config("gqa_decode", B=1, max_len=256, len_lo=1, len_hi=256)
+    gq_h, gkc_h, gvc_h, gsl_h = workloads.decode_inputs(gc, seed=rank)
+    gq, gkc, gvc, gsl = gq_h.to(dev), gkc_h.to(dev), gvc_h.to(dev), gsl_h.to(dev)
+    gout = torch.empty(gc["B"], gc["n_h"], gc["D_v"], dtype=torch.bfloat16, device=dev)
+    gws = torch.empty(attn.decode_workspace_size(gc["B"], gc["n_h"], gc["n_kv"], gc["D_qk"], gc["D_v"],
+                                                 gc["max_len"]), dtype=torch.uint8, device=dev)
+    mc = workloads.config("mla_decode")
+    if "mla" not in args.parts:
+        mc = workloads.config("mla_decode", B=1, max_len=256, len_lo=1, len_hi=256)
+    mq_h, mkc_h, _, msl_h = workloads.decode_inputs(mc, seed=rank)
+    mq, mkc, msl = mq_h.to(dev), mkc_h.to(dev), msl_h.to(dev)
+    mvc = mkc[..., :mc["D_v"]]
+    mout = torch.empty(mc["B"], mc["n_h"], mc["D_v"], dtype=torch.bfloat16, device=dev)
+    mws = torch.empty(attn.decode_workspace_size(mc["B"], mc["n_h"], mc["n_kv"], mc["D_qk"], mc["D_v"],
+                                                 mc["max_len"]), dtype=torch.uint8, device=dev)
+
+    def prefill():
+        attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot, stream=stream)
+
+    def gqa():
+        attn.decode(gq, gkc, gvc, gsl, rope_base=gc["rope_base"], rope_offset=0, rope_dims=gc["rope_dims"],
+                    scale=gc["scale"], out=gout, workspace=gws, stream=stream)
+
+    def mla():
+        attn.decode(mq, mkc, mvc, msl, rope_base=mc["rope_base"], rope_offset=mc["rope_offset"],
+                    rope_dims=mc["rope_dims"], scale=mc["scale"], out=mout, workspace=mws, stream=stream)
+
+    parts = [(n, fn) for n, fn in (("prefill", prefill), ("gqa", gqa), ("mla", mla)) if n in args.parts]
+    for _ in range(args.warmup):
+        for _, fn in parts:
+            fn()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, events around every call on the launching stream
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] for name, _ in parts}
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    launches0 = attn.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        for name, fn in parts:
+            a, b = ev[name][i]
+            a.record(stream)
+            fn()
+            b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = attn.launch_count() - launches0
+    clocks = sampler.stop()
+    if attn.device_status() != 0:
+        raise RuntimeError("a kernel reported a device-side wait timeout")
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    part_ms = {name: max_over_ranks(sum(a.elapsed_time(b) for a, b in ev[name]), world) / args.steps
+               for name, _ in parts}
+    for name in ("prefill", "gqa", "mla"):
+        part_ms.setdefault(name, float("nan"))
+    pf_flops = workloads.causal_flops(pc["B"], pc["S"], pc["n_h"], pc["D_h"])
+    g_bytes = workloads.decode_bytes(gc, gsl_h.tolist())
+    m_bytes = workloads.decode_bytes(mc, msl_h.tolist())
+    prefill_tflops = world * pf_flops / (part_ms["prefill"] * 1e-3) / 1e12
+    gqa_gbs = world * g_bytes / (part_ms["gqa"] * 1e-3) / 1e9
+    mla_gbs = world * m_bytes / (part_ms["mla"] * 1e-3) / 1e9
+    mla_tflops = world * workloads.decode_flops(mc, msl_h.tolist()) / (part_ms["mla"] * 1e-3) / 1e12
+
+    hbm_peak = float(peaks["hbm_gbs"])
+    bf16_peak = float(peaks["bf16_tflops"])
+    traffic = PREFILL_TRAFFIC["bytes"] if PREFILL_TRAFFIC["kernel_sha"] == kernel_sha("prefill_tc.cu") else None
+    per_gpu_prefill = prefill_tflops / world
+    roofline = {"bound": "tensor", "achieved": per_gpu_prefill, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": per_gpu_prefill / bf16_peak, "traffic": traffic,
+                "kernel": "attn_prefill (RoPE-K pass + prefill_tc_kernel<128>)",
+                "peak_source": f"{peak_kind} bf16 burst"}
+
+    # ---- end to end through the public API: pinned host inputs in, result out, every step
+    e2e = None
+    if not args.no_e2e and "prefill" in args.parts:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        outp = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            prefill()
+            outp.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+        e2e = {"value": world * pf_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outp.numel() * outp.element_size(),
+               "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(q_h, k_h, v_h, pc)
+        cpu["decode_gqa"] = cpu_baseline_decode(gq_h, gkc_h, gvc_h, gsl_h, gc, n_seq=4)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": prefill_tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
+                                   " + GQA decode 59 seqs L~U[4096,8192] n_h=32 n_kv=8 D_h=128"
+                                   " + MLA-absorbed decode 32 seqs x 32768 keys, 128 heads, 576/512 latent",
+                       "l2": "every input larger than L2 (129 MB); no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "parts": {
+                "prefill": {"ms": part_ms["prefill"], "value": prefill_tflops, "unit": "TFLOP/s",
+                            "frac_of_peak": per_gpu_prefill / bf16_peak},
+                "gqa_decode": {"ms": part_ms["gqa"], "value": gqa_gbs, "unit": "GB/s",
+                               "roofline": {"bound": "hbm", "achieved": gqa_gbs / world, "peak": hbm_peak,
+                                            "unit": "GB/s", "frac": gqa_gbs / world / hbm_peak}},
+                "mla_decode": {"ms": part_ms["mla"], "value": mla_gbs, "unit": "GB/s", "tflops": mla_tflops,
+                               "roofline": {"bound": "hbm", "achieved": mla_gbs / world, "peak": hbm_peak,
+                                            "unit": "GB/s", "frac": mla_gbs / world / hbm_peak}},
+            },
+            "roofline": roofline,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--parts", default="prefill,gqa,mla",
+                    help="comma-separated subset of prefill,gqa,mla (profiling runs)")
+    ap.add_argument("--prefill-batch", type=int, default=4,
+                    help="batch of the prefill workload (4 = the benchmark workload; smaller for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("at least 3 warm-up steps")
+    args.parts = [p for p in args.parts.split(",") if p]
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
