@@ -101,3 +101,45 @@ def test_decode_with_cache_matches_prefill_token_by_token(lib):
         ref = oracle.attention_prefill(q, k, v, rope_base=base)[:, t]
         assert_parity(out, ref, "bf16", f"decode t={t}")
         assert_parity(out, to_np(full[:, t]), "bf16", f"decode vs prefill t={t}")
+
+
+MLA_SMALL = [
+    # B, max_len, rope_base: 128 heads over one 576-dim latent head, the tensor-core MLA kernel
+    (3, 300, 0.0),
+    (5, 100, 1e4),      # RoPE on the last 64 latent dims
+    (40, 64, 0.0),      # many short sequences: key ranges of CTA pairs cross sequence ends
+    (1, 2000, 0.0),     # one sequence split over every pair
+]
+
+
+@pytest.mark.parametrize("B,L,rope", MLA_SMALL)
+def test_mla_shaped_decode(lib, B, L, rope):
+    cfg = workloads.config("mla_decode", B=B, max_len=L, len_lo=1, len_hi=L, rope_base=rope)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=B * 7 + L)
+    sl[0] = 1
+    sl[-1] = L
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", f"mla B={B} L={L}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode"])
+def test_rows_past_seqlens_are_never_used(lib, name):
+    # cache rows at or after seqlens[b] hold NaN: results must still match the oracle
+    if name == "gqa_decode":
+        cfg = workloads.config(name, B=4, max_len=300, len_lo=1, len_hi=300)
+    else:
+        cfg = workloads.config(name, B=4, max_len=200, len_lo=1, len_hi=200)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=21)
+    sl[0] = 1
+    kc_n = kc.clone()
+    vc_n = kc_n[..., :cfg["D_v"]] if cfg.get("v_aliases_k") else vc.clone()
+    for b in range(cfg["B"]):
+        kc_n[b, int(sl[b]):] = float("nan")
+        if not cfg.get("v_aliases_k"):
+            vc_n[b, int(sl[b]):] = float("nan")
+    out, _ = run_decode(lib, cfg, q, kc_n, vc_n, sl)
+    assert torch.isfinite(out).all()
+    ref, _ = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", f"{name} with NaN past seqlens")
