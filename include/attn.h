@@ -100,6 +100,46 @@ ATTN_API int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads,
               attn_dtype_t dtype, void* stream);
 
 /*
+ * attn_prefill_chunk - a chunk of a prompt whose earlier keys are already in a
+ * KV cache (chunked prefill, "Transformer 与 LLM" slide 07: a long prompt is
+ * split so that one request does not hold the GPU).  Query row m of the chunk
+ * sits at absolute position q_offset + m and, when causal, attends cache keys
+ * 0 .. q_offset + m ("2.7 Transformer Decoder Block完整解析" §3.2); without the
+ * mask it attends keys 0 .. q_offset + S_q - 1.
+ *
+ *   q       [B, S_q, n_h, D_h]       the chunk's queries, NOT rotated (rotated here
+ *                                    at their absolute positions when rope_base > 0).
+ *   kcache  [B, max_len, n_kv, D_h]  rotated keys; rows 0 .. q_offset + S_q - 1 must
+ *                                    already hold this chunk's keys too (attn_kv_append).
+ *   vcache  [B, max_len, n_kv, D_h]  values, same layout.
+ *   out     [B, S_q, n_h, D_h]; lse optional fp32 [B, n_h, S_q].
+ * Requires 0 <= q_offset and q_offset + S_q <= max_len.  Other arguments,
+ * dtypes and errors as attn_prefill.  Rows past q_offset + S_q are never read.
+ */
+ATTN_API int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, void* out, float* lse,
+                                int B, int S_q, int q_offset, int max_len, int n_h, int n_kv, int D_h,
+                                float rope_base, float scale, int causal, attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_kv_append - write C new tokens per sequence into a KV cache: key row c
+ * of sequence b is rotated at absolute position start[b] + c (the cache keeps
+ * rotated keys, "Transformer架构完全深度解析" §7) and stored in that slot, its value
+ * row is copied next to it (§9: K_cache = concat(K_cache, K_new)).
+ *
+ *   k_new   [B, C, n_kv, D_qk]; v_new [B, C, n_kv, D_v], or NULL when values
+ *           alias the keys (MLA: V is the first D_v dims of the stored row).
+ *   kcache  [B, max_len, n_kv, D_qk]; vcache with token stride v_token_stride
+ *           (0 = n_kv * D_v), as in attn_decode.
+ *   start   DEVICE int32 [B]: slot of the first new token of each sequence (for
+ *           one decode step: seqlens[b] - 1).  Slots outside [0, max_len) are skipped.
+ *   rope_base > 0 rotates dims [rope_offset, rope_offset + rope_dims) of the keys.
+ * D_qk, D_v, rope_offset and rope_dims must be multiples of 8.
+ */
+ATTN_API int attn_kv_append(const void* k_new, const void* v_new, void* kcache, void* vcache, int v_token_stride,
+                            const int* start, int B, int C, int n_kv, int D_qk, int D_v, int max_len,
+                            float rope_base, int rope_offset, int rope_dims, attn_dtype_t dtype, void* stream);
+
+/*
  * attn_decode_workspace_size - bytes of device scratch attn_decode needs for
  * these sizes (0 is never returned for valid sizes; -1 cast to size_t for
  * invalid ones).  The caller allocates it; it may be reused across calls that

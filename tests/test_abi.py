@@ -35,7 +35,7 @@ def declared_symbols():
 def test_header_and_binding_agree():
     names = set(declared_symbols())
     assert names == {n for n, _, _ in B.SIGNATURES}
-    assert len(names) == 8
+    assert len(names) == 10
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -121,3 +121,26 @@ def test_wait_limit_and_counter(lib):
     before = lib.attn_launch_count()
     lib.attn_set_wait_limit_ns(2_000_000_000)
     assert lib.attn_launch_count() == before
+
+
+def test_prefill_chunk_argument_errors(lib):
+    f = lib.attn_prefill_chunk
+    # q, kc, vc, out, lse, B, S_q, q_offset, max_len, n_h, n_kv, D, rope, scale, causal, dtype, stream
+    assert f(None, FAKE, FAKE, FAKE, None, 1, 16, 0, 64, 2, 2, 64, 0.0, 0.0, 1, 1, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 16, 60, 64, 2, 2, 64, 0.0, 0.0, 1, 1, None) == -1  # past max_len
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 16, -1, 64, 2, 2, 64, 0.0, 0.0, 1, 1, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 16, 0, 64, 3, 2, 64, 0.0, 0.0, 1, 1, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 16, 0, 64, 2, 2, 264, 0.0, 0.0, 1, 1, None) == -2
+    assert f(MISALIGNED, FAKE, FAKE, FAKE, None, 1, 16, 0, 64, 2, 2, 64, 0.0, 0.0, 1, 1, None) == -3
+
+
+def test_kv_append_argument_errors(lib):
+    f = lib.attn_kv_append
+    # k_new, v_new, kc, vc, ldv, start, B, C, n_kv, D_qk, D_v, max_len, rope, roff, rdims, dtype, stream
+    assert f(None, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 0.0, 0, 64, 1, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, None, 1, 1, 2, 64, 64, 16, 0.0, 0, 64, 1, None) == -1
+    assert f(FAKE, FAKE, FAKE, None, 0, FAKE, 1, 1, 2, 64, 64, 16, 0.0, 0, 64, 1, None) == -1   # v_new without vcache
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 60, 64, 16, 0.0, 0, 64, 1, None) == -1   # D not a multiple of 8
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 1e4, 4, 56, 1, None) == -1   # offset not a multiple of 8
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 1e4, 32, 64, 1, None) == -1  # span past D_qk
+    assert f(MISALIGNED, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 0.0, 0, 64, 1, None) == -3

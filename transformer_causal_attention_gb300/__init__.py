@@ -11,6 +11,8 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     decode,
     decode_workspace_size,
+    kv_append,
+    prefill_chunk,
     device_status,
     launch_count,
     load,

@@ -28,6 +28,8 @@ SIGNATURES = [
     ("attn_strerror", ctypes.c_char_p, [_i]),
     ("attn_prefill", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
     ("attn_rope", _i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    ("attn_prefill_chunk", _i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
+    ("attn_kv_append", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     ("attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i, _i, _i]),
     ("attn_decode", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
                          _vp, _sz, _vp]),
@@ -146,6 +148,57 @@ def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = N
                           _dtype_code(x), _stream_ptr(stream))
     _check(rc, "attn_rope")
     return out
+
+
+def prefill_chunk(q, kcache, vcache, *, q_offset: int, rope_base: float = 0.0, scale: float = 0.0,
+                  causal: bool = True, out=None, lse: bool = False, stream=None):
+    """A prompt chunk at positions q_offset.. against a KV cache via attn_prefill_chunk.
+
+    q [B,S_q,n_h,D] (un-rotated), kcache/vcache [B,max_len,n_kv,D] holding rotated keys
+    0 .. q_offset+S_q-1 (this chunk's included).  Returns (out [B,S_q,n_h,D], lse or None).
+    """
+    for name, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _dev(t, name)
+    B, S_q, n_h, D = q.shape
+    max_len, n_kv = kcache.shape[1], kcache.shape[2]
+    if vcache.shape != kcache.shape:
+        raise ValueError("vcache must match kcache")
+    if out is None:
+        out = torch.empty_like(q)
+    lse_t = torch.empty((B, n_h, S_q), dtype=torch.float32, device=q.device) if lse else None
+    rc = _lib().attn_prefill_chunk(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), _ptr(lse_t), B, S_q, q_offset,
+                                   max_len, n_h, n_kv, D, float(rope_base), float(scale), 1 if causal else 0,
+                                   _dtype_code(q), _stream_ptr(stream))
+    _check(rc, "attn_prefill_chunk")
+    return out, lse_t
+
+
+def kv_append(k_new, v_new, kcache, vcache, start, *, rope_base: float = 0.0, rope_offset: int = 0,
+              rope_dims: int | None = None, stream=None):
+    """Write new tokens into a KV cache via attn_kv_append (keys rotated at start[b] + c).
+
+    k_new [B,C,n_kv,D_qk], v_new [B,C,n_kv,D_v] or None (values alias the keys),
+    kcache [B,max_len,n_kv,D_qk], vcache contiguous or a leading slice of kcache's
+    last dim, start int32 [B] on the device.
+    """
+    _dev(k_new, "k_new")
+    _dev(kcache, "kcache")
+    if not start.is_cuda or start.dtype != torch.int32:
+        raise ValueError("start must be an int32 CUDA tensor")
+    B, C, n_kv, D_qk = k_new.shape
+    max_len = kcache.shape[1]
+    if v_new is not None:
+        _dev(v_new, "v_new")
+        D_v = v_new.shape[-1]
+        ldv = 0 if vcache.is_contiguous() else vcache.stride(1)
+    else:
+        D_v = vcache.shape[-1] if vcache is not None else D_qk
+        ldv = 0
+    rope_dims = (D_qk - rope_offset) if rope_dims is None else rope_dims
+    rc = _lib().attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kcache), None if vcache is None else vcache.data_ptr(),
+                               ldv, _ptr(start), B, C, n_kv, D_qk, D_v, max_len, float(rope_base), rope_offset,
+                               rope_dims, _dtype_code(k_new), _stream_ptr(stream))
+    _check(rc, "attn_kv_append")
 
 
 def decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len, dtype=torch.bfloat16) -> int:

@@ -62,21 +62,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D tensor map over a BSHD bf16 tensor [B, S, heads, D]: boxes of
-// 64 head-dims x 1 head x 128 positions x 1 batch, 128-byte swizzle (the
-// canonical K-major layout of the tensor-core operands), zero fill outside.
-bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D) {
+// 4-D tensor map over a bf16 tensor indexed (d, head, position, batch) with
+// the given byte strides of head / position / batch: boxes of 64 dims x 1 head x
+// box_rows positions x 1 batch, 128-byte swizzle (the canonical K-major operand
+// layout of the tensor cores), zero fill outside the tensor.
+bool make_map4(CUtensorMap* map, const void* base, int D, int heads, int rows, int B, unsigned long long head_stride,
+               unsigned long long row_stride, unsigned long long batch_stride, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
-                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(heads) * D * 2,
-                                 static_cast<cuuint64_t>(S) * heads * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+                              static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {head_stride, row_stride, batch_stride};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D tensor map over a bf16 tensor indexed (d, row, batch): boxes of 64 dims x
+// box_rows rows x 1 batch, 128-byte swizzle, zero fill outside.
+bool make_map3(CUtensorMap* map, const void* base, int D, int rows, int B, unsigned long long row_stride,
+               unsigned long long batch_stride, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {row_stride, batch_stride};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MLA shape served by the tensor-core decode kernel (one 576-dim latent head, V = its first 512 dims).
+bool mla_shape(int B, int n_h, int n_kv, int D_qk, int D_v, attn_dtype_t dtype) {
+  return dtype == ATTN_BF16 && n_h == 128 && n_kv == 1 && D_qk == 576 && D_v == 512 && B <= 1024;
+}
+
+// Dense BSHD tensor [B, S, heads, D], boxes of 128 positions.
+bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D) {
+  const unsigned long long hs = static_cast<unsigned long long>(D) * 2;
+  return make_map4(map, base, D, heads, S, B, hs, hs * heads, hs * heads * S, 128);
 }
 
 // theta_i = base^(-2i/dims) expressed in turns per position, split hi + lo.
@@ -178,7 +205,7 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k
     if (e != cudaSuccess) return finish(e, launches);
   }
   PrefillArgs pa{q, rope ? k_rot : k, v, out, lse, B, S, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
-                 g_wait_limit_ns.load()};
+                 g_wait_limit_ns.load(), S, 0, S};
   if (prefill_tc_supported(D_h, bf16)) {
     CUtensorMap maps[3];
     if (!make_bshd_map(&maps[0], q, B, S, n_h, D_h) || !make_bshd_map(&maps[1], pa.k, B, S, n_kv, D_h) ||
@@ -191,12 +218,78 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k
   return finish(e, launches);
 }
 
+int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, void* out, float* lse, int B, int S_q,
+                       int q_offset, int max_len, int n_h, int n_kv, int D_h, float rope_base, float scale,
+                       int causal, attn_dtype_t dtype, void* stream) {
+  if (!q || !kcache || !vcache || !out) return ATTN_ERR_ARG;
+  if (B <= 0 || S_q <= 0 || n_h <= 0 || n_kv <= 0 || D_h <= 0 || n_h % n_kv) return ATTN_ERR_ARG;
+  if (q_offset < 0 || max_len <= 0 || static_cast<long long>(q_offset) + S_q > max_len) return ATTN_ERR_ARG;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  const bool bf16 = dtype == ATTN_BF16;
+  if (D_h > 256 || D_h % (bf16 ? 8 : 2)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_ALIGN;
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_h));
+  const int S_k = q_offset + S_q;
+  PrefillArgs pa{q, kcache, vcache, out, lse, B, S_q, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
+                 g_wait_limit_ns.load(), S_k, q_offset, max_len};
+  const RopeFreq rf = make_rope(rope_base, D_h);
+  int launches = 0;
+  cudaError_t e;
+  if (prefill_tc_supported(D_h, bf16)) {
+    // K/V maps cover only the S_k visible rows of each sequence: rows past them read as zero
+    CUtensorMap maps[3];
+    const unsigned long long hs = static_cast<unsigned long long>(D_h) * 2;
+    if (!make_bshd_map(&maps[0], q, B, S_q, n_h, D_h) ||
+        !make_map4(&maps[1], kcache, D_h, n_kv, S_k, B, hs, hs * n_kv, hs * n_kv * max_len, 128) ||
+        !make_map4(&maps[2], vcache, D_h, n_kv, S_k, B, hs, hs * n_kv, hs * n_kv * max_len, 128))
+      return finish(cudaErrorInvalidValue, launches);
+    e = launch_prefill_tc(pa, rf, maps, dev.sms, st, &launches);
+  } else {
+    e = launch_prefill_simt(pa, rf, bf16, st, &launches);
+  }
+  return finish(e, launches);
+}
+
+int attn_kv_append(const void* k_new, const void* v_new, void* kcache, void* vcache, int v_token_stride,
+                   const int* start, int B, int C, int n_kv, int D_qk, int D_v, int max_len, float rope_base,
+                   int rope_offset, int rope_dims, attn_dtype_t dtype, void* stream) {
+  if (!k_new || !kcache || !start || (v_new && !vcache)) return ATTN_ERR_ARG;
+  if (B <= 0 || C <= 0 || n_kv <= 0 || D_qk <= 0 || D_v <= 0 || max_len <= 0 || v_token_stride < 0)
+    return ATTN_ERR_ARG;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  if (D_qk % 8 || D_v % 8) return ATTN_ERR_ARG;
+  const bool rope = rope_base > 0.f;
+  if (rope && (rope_offset < 0 || rope_dims <= 0 || rope_offset % 8 || rope_dims % 8 || rope_offset + rope_dims > D_qk))
+    return ATTN_ERR_ARG;
+  if (rope && rope_dims / 2 > kMaxRopePairs) return ATTN_ERR_UNSUPPORTED;
+  const long long ldv = v_token_stride ? v_token_stride : static_cast<long long>(n_kv) * D_v;
+  if (!aligned16(k_new) || !aligned16(kcache) || (v_new && (!aligned16(v_new) || !aligned16(vcache))) ||
+      (reinterpret_cast<uintptr_t>(start) & 3u))
+    return ATTN_ERR_ALIGN;
+  KvAppendArgs ka{k_new, v_new, kcache, vcache, ldv, start, B, C, n_kv, D_qk, D_v, max_len, rope ? rope_offset : 0};
+  int launches = 0;
+  const cudaError_t e = launch_kv_append(ka, make_rope(rope_base, rope ? rope_dims : 0), dtype == ATTN_BF16,
+                                         static_cast<cudaStream_t>(stream), &launches);
+  return finish(e, launches);
+}
+
 size_t attn_decode_workspace_size(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, attn_dtype_t dtype) {
   if (B <= 0 || n_h <= 0 || n_kv <= 0 || n_h % n_kv || D_qk <= 0 || D_v <= 0 || max_len <= 0) return static_cast<size_t>(-1);
   if (dtype != ATTN_F32 && dtype != ATTN_BF16) return static_cast<size_t>(-1);
   int chunk = 0;
   const int ns = decode_plan_splits(B, n_h, n_kv, D_qk, D_v, max_len, &chunk);
-  const size_t slots = static_cast<size_t>(B) * n_h * ns;
+  size_t slots = static_cast<size_t>(B) * n_h * ns;
+  if (mla_shape(B, n_h, n_kv, D_qk, D_v, dtype)) {
+    // one partial per (pair, sequence) piece: at most pairs + B - 1 of them
+    const size_t mla_slots = static_cast<size_t>(kMlaMaxPairs + B) * n_h;
+    if (mla_slots > slots) slots = mla_slots;
+  }
   const size_t o_bytes = (slots * D_v * sizeof(float) + 255) & ~size_t(255);
   return o_bytes + ((slots * sizeof(float) + 255) & ~size_t(255));
 }
@@ -227,17 +320,50 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, int v_tok
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
   int chunk = 0;
-  const int ns = decode_plan_splits(B, n_h, n_kv, D_qk, D_v, max_len, &chunk);
-  const size_t slots = static_cast<size_t>(B) * n_h * ns;
+  int ns = decode_plan_splits(B, n_h, n_kv, D_qk, D_v, max_len, &chunk);
+  size_t slots = static_cast<size_t>(B) * n_h * ns;
+  if (mla_shape(B, n_h, n_kv, D_qk, D_v, dtype)) {
+    const size_t mla_slots = static_cast<size_t>(kMlaMaxPairs + B) * n_h;
+    if (mla_slots > slots) slots = mla_slots;
+  }
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            ((slots * D_v * sizeof(float) + 255) & ~size_t(255)));
+  const bool use_mla = mla_shape(B, n_h, n_kv, D_qk, D_v, dtype) &&
+                       decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, dtype == ATTN_BF16) &&
+                       (!rope || (rope_offset % 8 == 0 && rope_dims % 8 == 0));
+  if (use_mla) {
+    ns = decode_mla_pairs(dev.sms);  // the kernel runs 2 CTAs per pair
+    chunk = 0;
+  }
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_qk));
   DecodeArgs da{q, kcache, vcache, ldv, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
                 rope ? rope_offset : 0, sc * kLog2e, ws_o, ws_lse, ns, chunk, dev.status, g_wait_limit_ns.load()};
   int launches = 0;
-  const cudaError_t e = launch_decode(da, make_rope(rope_base, rope ? rope_dims : 0), dtype == ATTN_BF16,
-                                      static_cast<cudaStream_t>(stream), &launches);
+  const bool bf16 = dtype == ATTN_BF16;
+  const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (use_mla) {
+    CUtensorMap maps[2];
+    const unsigned long long row = static_cast<unsigned long long>(D_qk) * 2;
+    if (!make_map3(&maps[0], q, D_qk, n_h, B, row, row * n_h, 128) ||
+        !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, 32))
+      return finish(cudaErrorInvalidValue, launches);
+    e = launch_decode_mla(da, rf, maps, st, &launches);
+  } else if (decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
+    // K and V stream through shared memory in 64-key tiles
+    CUtensorMap maps[2];
+    const unsigned long long ks = static_cast<unsigned long long>(D_qk) * 2;
+    const unsigned long long vs = static_cast<unsigned long long>(ldv) * 2;
+    if (!make_map4(&maps[0], kcache, D_qk, n_kv, max_len, B, ks, ks * n_kv, ks * n_kv * max_len, 64) ||
+        !make_map4(&maps[1], vcache, D_v, n_kv, max_len, B, static_cast<unsigned long long>(D_v) * 2, vs,
+                   vs * max_len, 64))
+      return finish(cudaErrorInvalidValue, launches);
+    e = launch_decode_stream(da, rf, maps, dev.sms, st, &launches);
+  } else {
+    e = launch_decode(da, rf, bf16, st, &launches);
+  }
   return finish(e, launches);
 }
 

@@ -303,13 +303,9 @@ cudaError_t launch_hg(const DecodeArgs& a, const RopeFreq& f, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_t(const DecodeArgs& a, const RopeFreq& f, cudaStream_t st) {
   const int nq = (a.D_qk + 127) / 128, nv = (a.D_v + 127) / 128;
-  cudaError_t e;
-  if (nq == 1 && nv == 1) e = launch_hg<T, 1, 1>(a, f, st);
-  else if (nq <= 2 && nv <= 2) e = launch_hg<T, 2, 2>(a, f, st);
-  else e = launch_hg<T, 5, 4>(a, f, st);
-  if (e != cudaSuccess) return e;
-  decode_combine_kernel<T><<<a.B * a.n_h, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  if (nq == 1 && nv == 1) return launch_hg<T, 1, 1>(a, f, st);
+  if (nq <= 2 && nv <= 2) return launch_hg<T, 2, 2>(a, f, st);
+  return launch_hg<T, 5, 4>(a, f, st);
 }
 
 }  // namespace
@@ -331,9 +327,20 @@ int decode_plan_splits(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len,
   return ns;
 }
 
+cudaError_t launch_decode_combine(const DecodeArgs& a, bool bf16, cudaStream_t st, int* launches) {
+  if (bf16)
+    decode_combine_kernel<__nv_bfloat16><<<a.B * a.n_h, 128, 0, st>>>(a);
+  else
+    decode_combine_kernel<float><<<a.B * a.n_h, 128, 0, st>>>(a);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches) {
-  *launches += 2;
-  return bf16 ? launch_t<__nv_bfloat16>(a, rope, st) : launch_t<float>(a, rope, st);
+  *launches += 1;
+  const cudaError_t e = bf16 ? launch_t<__nv_bfloat16>(a, rope, st) : launch_t<float>(a, rope, st);
+  if (e != cudaSuccess) return e;
+  return launch_decode_combine(a, bf16, st, launches);
 }
 
 }  // namespace attn

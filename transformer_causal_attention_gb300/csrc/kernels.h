@@ -16,11 +16,14 @@ struct PrefillArgs {
   const void* v;
   void* out;
   float* lse;  // nullable
-  int B, S, n_h, n_kv, D;
+  int B, S, n_h, n_kv, D;  // S = query rows per sequence
   float scale_log2;  // score multiplier times log2(e)
   int causal;
   unsigned int* status;
   unsigned long long wait_limit_ns;
+  int S_k;           // keys visible per sequence (keys 0 .. S_k-1)
+  int q_offset;      // absolute position of query row 0 (a chunk continuing a cache)
+  int kv_rows;       // rows per sequence in the K/V buffers (S for a prompt, max_len for a cache)
 };
 
 struct DecodeArgs {
@@ -47,6 +50,16 @@ struct RopeArgs {
   int B, S, n_heads, D, rope_offset, rope_dims, pos_offset;
 };
 
+struct KvAppendArgs {
+  const void* k_new;  // [B, C, n_kv, D_qk]
+  const void* v_new;  // [B, C, n_kv, D_v] or null (values alias the keys)
+  void* kcache;       // [B, max_len, n_kv, D_qk]
+  void* vcache;       // token stride v_token_stride elements
+  long long v_token_stride;
+  const int* start;   // device [B]: slot of the first new token of each sequence
+  int B, C, n_kv, D_qk, D_v, max_len, rope_offset;
+};
+
 // Each launcher returns the launch error (cudaSuccess when enqueued) and adds
 // the number of kernels it enqueued to *launches.
 cudaError_t launch_prefill_simt(const PrefillArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
@@ -55,8 +68,19 @@ bool prefill_tc_supported(int D, bool bf16);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps,
                               int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_rope(const RopeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches);
+cudaError_t launch_kv_append(const KvAppendArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches);
 int decode_plan_splits(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, int* chunk);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
                           int* launches);
+cudaError_t launch_decode_combine(const DecodeArgs& a, bool bf16, cudaStream_t st, int* launches);
+constexpr int kMlaMaxPairs = 128;  // CTA pairs of the MLA decode kernel (workspace is sized for this)
+bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long v_token_stride, bool v_is_k,
+                          bool bf16);
+int decode_mla_pairs(int num_sms);
+cudaError_t launch_decode_mla(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, cudaStream_t st,
+                              int* launches);
+bool decode_stream_supported(int n_h, int n_kv, int D_qk, int D_v, bool bf16);
+cudaError_t launch_decode_stream(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
+                                 cudaStream_t st, int* launches);
 
 }  // namespace attn

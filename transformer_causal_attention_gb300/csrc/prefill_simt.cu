@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(PrefillArgs a, RopeFr
     float x0 = to_f32(qrow[2 * i]), x1 = to_f32(qrow[2 * i + 1]);
     if (f.n_pairs) {
       float s, c;
-      rope_sincos(m, f.hi[i], f.lo[i], &s, &c);
+      rope_sincos(a.q_offset + m, f.hi[i], f.lo[i], &s, &c);
       rotate_pair(x0, x1, s, c);
     }
     q_s[warp][2 * i] = x0 * a.scale_log2;
@@ -56,14 +56,14 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(PrefillArgs a, RopeFr
   __syncwarp();
 
   const long long row_stride = static_cast<long long>(a.n_kv) * D;  // between consecutive keys
-  const T* kbase = static_cast<const T*>(a.k) + (static_cast<long long>(b) * a.S * a.n_kv + g) * D;
-  const T* vbase = static_cast<const T*>(a.v) + (static_cast<long long>(b) * a.S * a.n_kv + g) * D;
+  const T* kbase = static_cast<const T*>(a.k) + (static_cast<long long>(b) * a.kv_rows * a.n_kv + g) * D;
+  const T* vbase = static_cast<const T*>(a.v) + (static_cast<long long>(b) * a.kv_rows * a.n_kv + g) * D;
   constexpr int NT = DMAX / 32;
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
   float m_run = -INFINITY, l = 0.f;
-  const int n_end = a.causal ? m + 1 : a.S;
+  const int n_end = a.causal ? a.q_offset + m + 1 : a.S_k;
 
   for (int n0 = 0; n0 < n_end; n0 += 32) {
     const int n = n0 + lane;

@@ -67,6 +67,12 @@ struct Item {
   int b, h, g, qt0, n0, n1;
 };
 
+// Key tiles a causal Q tile needs: up to the tile holding its last query's position.
+__device__ __forceinline__ int causal_tiles(int qt, const PrefillArgs& a) {
+  const int last_row = min(qt * BM + BM - 1, a.S - 1);
+  return (a.q_offset + last_row) / BN + 1;
+}
+
 __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n_pairs_q, int n_kt) {
   Item it;
   const int bh_count = a.B * a.n_h;
@@ -77,8 +83,8 @@ __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n
   it.g = it.h / (a.n_h / a.n_kv);
   it.qt0 = 2 * p;
   if (a.causal) {
-    it.n0 = min(it.qt0 + 1, n_kt);
-    it.n1 = min(it.qt0 + 2, n_kt);
+    it.n0 = causal_tiles(it.qt0, a);
+    it.n1 = causal_tiles(it.qt0 + 1, a);
   } else {
     it.n0 = it.n1 = n_kt;
   }
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_qt = (a.S + BM - 1) / BM;
-  const int n_kt = (a.S + BN - 1) / BN;
+  const int n_kt = (a.S_k + BN - 1) / BN;
   const int n_pairs_q = (n_qt + 1) / 2;
   const int n_items = a.B * a.n_h * n_pairs_q;
 
@@ -297,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
       const int n_t = t ? itm.n1 : itm.n0;
-      const int m = qt * BM + r;  // query position
+      const int m = qt * BM + r;  // query row
+      const int pos = a.q_offset + m;  // its absolute position
       if (!warp_wait(&bars->q_full[t], it & 1, wc)) break;
       if (f.n_pairs) {
         // rotate this thread's query row in place (swizzled layout: the 16-byte
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float sn, cs;
-            rope_sincos(m, f.hi[c * 4 + e], f.lo[c * 4 + e], &sn, &cs);
+            rope_sincos(pos, f.hi[c * 4 + e], f.lo[c * 4 + e], &sn, &cs);
             rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
           }
           *p = f32_to_bf16x8(x);
@@ -334,19 +341,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
         const int key0 = j * BN;
-        if (a.causal && j == qt) {
+        if (a.causal && key0 + BN - 1 > a.q_offset + qt * BM) {
+          // some key of this tile lies after some query of the Q tile: mask key > position
 #pragma unroll
           for (int c = 0; c < BN; ++c)
-            if (c > r) s[c] = -INFINITY;
-        } else if (!a.causal && key0 + BN > a.S) {
+            if (key0 + c > pos) s[c] = -INFINITY;
+        } else if (!a.causal && key0 + BN > a.S_k) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)
-            if (key0 + c >= a.S) s[c] = -INFINITY;
+            if (key0 + c >= a.S_k) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row maximum: 8 independent chains, then a tree (a single chain of 127
+        // dependent max operations would dominate the warp's latency)
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-        mx *= a.scale_log2;
+        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+#pragma unroll
+        for (int w2 = 4; w2 > 0; w2 >>= 1)
+#pragma unroll
+          for (int i = 0; i < w2; ++i) m8[i] = fmaxf(m8[i], m8[i + w2]);
+        const float mx = m8[0] * a.scale_log2;
         // Move to a new reference maximum only when the row maximum grew by more
         // than the threshold; O and l are then scaled by alpha = 2^(m_old - m_new).
         const bool need = mx > m_run + kRescaleThreshold;
@@ -369,16 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_addr + c * 32, orow);
           }
         }
+        // p = 2^(s * scale*log2e - m), two columns per packed fp32x2 FMA; the row
+        // sum runs in 4 independent packed accumulators
         uint32_t pr[BN / 2];
-        float rs = 0.f;
+        const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
-          const float p0 = fast_exp2(fmaf(s[2 * c], a.scale_log2, -m_run));
-          const float p1 = fast_exp2(fmaf(s[2 * c + 1], a.scale_log2, -m_run));
-          rs += p0 + p1;
-          pr[c] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[c & 3] = __fadd2_rn(acc[c & 3], pp);
+          pr[c] = pack_bf16x2(pp.x, pp.y);
         }
-        l_run += rs;
+        acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l_run += acc[0].x + acc[0].y;
         tmem_st32(s_addr, pr);
         tmem_st32(s_addr + 32, pr + 32);
         tmem_wait_st();
