@@ -183,6 +183,41 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, 
                 void* stream);
 
 /*
+ * attn_decode_static - attn_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point: it exists for
+ * callers that are not allowed to call cudaMalloc (or anything that does) when
+ * they run a decode step - for example an inference-engine plugin whose
+ * per-step hook must not allocate because the engine owns all device memory,
+ * a latency-critical token loop that cannot afford the device-wide
+ * synchronisation cudaMalloc/cudaFree may cause, or a runtime whose device
+ * memory budget is fixed at start-up.  Such a caller cannot provide
+ * attn_decode's workspace, so this variant keeps the split-KV partial results
+ * in a scratch array compiled into the library instead:
+ *  - the array is ATTN_DECODE_STATIC_SCRATCH_BYTES (16 MiB) of device memory
+ *    that every GPU holds from the moment the library is loaded on it until
+ *    the process exits, whether or not this function is ever called;
+ *  - a problem whose attn_decode_workspace_size(...) exceeds that size is
+ *    rejected with ATTN_ERR_WORKSPACE before anything is launched (for
+ *    example the GQA decode of 59 sequences x 8192 keys, n_h = 32, n_kv = 8,
+ *    D = 128 fits; the 32 x 32768-key MLA decode does not);
+ *  - the first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture;
+ *  - every call on a device shares the one array and it keeps whatever the
+ *    last call left in it.  Nothing in it needs to start at zero (each call
+ *    writes every partial it later reads), but calls whose kernels can overlap
+ *    on the GPU - on different streams without ordering between them - race on
+ *    the array and give wrong results: order them.
+ * Arguments, layouts, results and errors are those of attn_decode, minus the
+ * workspace pair.  No device memory is allocated or freed.
+ */
+#define ATTN_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+ATTN_API int attn_decode_static(const void* q, const void* kcache, const void* vcache, int v_token_stride,
+                                const int* seqlens, void* out, float* lse, int B, int n_h, int n_kv, int D_qk,
+                                int D_v, int max_len, float rope_base, int rope_offset, int rope_dims,
+                                float scale, attn_dtype_t dtype, void* stream);
+
+/*
  * attn_device_status - synchronise the stream, then return ATTN_OK, or
  * ATTN_ERR_TIMEOUT if a kernel of this library gave up on a bounded wait since
  * the last call (the flag is cleared), or ATTN_ERR_CUDA if the stream reports

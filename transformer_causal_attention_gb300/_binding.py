@@ -33,6 +33,8 @@ SIGNATURES = [
     ("attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i, _i, _i]),
     ("attn_decode", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
                          _vp, _sz, _vp]),
+    ("attn_decode_static", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
+                                _vp]),
     ("attn_device_status", _i, [_vp]),
     ("attn_launch_count", _u64, []),
     ("attn_set_wait_limit_ns", None, [_u64]),

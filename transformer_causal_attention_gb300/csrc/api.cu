@@ -367,6 +367,56 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, int v_tok
   return finish(e, launches);
 }
 
+// ---------------------------------------------------------------------------
+// Decode with library-owned scratch, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace attn {
+namespace {
+
+// File-scope scratch of attn_decode_static: one per device that loads the
+// library, shared by every call on that device.  In host code the name is only
+// a stand-in; the device address comes from cudaGetSymbolAddress below.
+__device__ __align__(256) unsigned char g_decode_scratch[ATTN_DECODE_STATIC_SCRATCH_BYTES];
+
+void* g_scratch_addr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device with that device current.
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_decode_static(const void* q, const void* kcache, const void* vcache, int v_token_stride, const int* seqlens,
+                       void* out, float* lse, int B, int n_h, int n_kv, int D_qk, int D_v, int max_len,
+                       float rope_base, int rope_offset, int rope_dims, float scale, attn_dtype_t dtype,
+                       void* stream) {
+  const size_t need = attn_decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len, dtype);
+  if (need == static_cast<size_t>(-1)) return ATTN_ERR_ARG;
+  if (need > ATTN_DECODE_STATIC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (int rc = static_scratch(&scratch)) return rc;
+  return attn_decode(q, kcache, vcache, v_token_stride, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
+                     rope_base, rope_offset, rope_dims, scale, dtype, scratch, ATTN_DECODE_STATIC_SCRATCH_BYTES,
+                     stream);
+}
+
 int attn_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
