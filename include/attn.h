@@ -100,6 +100,19 @@ ATTN_API int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads,
               attn_dtype_t dtype, void* stream);
 
 /*
+ * attn_prefill_window - attn_prefill with a causal sliding window and
+ * attention sinks ("Transformer 与 LLM" slide 07: a window of W keys turns the
+ * O(s) KV and compute of each query into O(W); keeping the first few tokens -
+ * the sinks - preserves the start of the sequence).  A query at position m sees
+ * key n when n <= m and (m - n < window or n < n_sink).  Key tiles that hold no
+ * visible key for a query tile are skipped.  window > 0 is required; other
+ * arguments as attn_prefill (the mask is always causal).
+ */
+ATTN_API int attn_prefill_window(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse,
+                                 int B, int S, int n_h, int n_kv, int D_h, float rope_base, float scale, int window,
+                                 int n_sink, attn_dtype_t dtype, void* stream);
+
+/*
  * attn_prefill_chunk - a chunk of a prompt whose earlier keys are already in a
  * KV cache (chunked prefill, "Transformer 与 LLM" slide 07: a long prompt is
  * split so that one request does not hold the GPU).  Query row m of the chunk
@@ -183,6 +196,19 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, 
                 void* stream);
 
 /*
+ * attn_decode_window - attn_decode with a sliding window and attention sinks
+ * ("Transformer 与 LLM" slide 07): the new token at position L-1 sees cached
+ * keys n with L-1-n < window, plus the first n_sink keys.  Key chunks with no
+ * visible key are not read.  window > 0 is required; everything else as
+ * attn_decode (same workspace size).
+ */
+ATTN_API int attn_decode_window(const void* q, const void* kcache, const void* vcache, int v_token_stride,
+                                const int* seqlens, void* out, float* lse, int B, int n_h, int n_kv, int D_qk,
+                                int D_v, int max_len, float rope_base, int rope_offset, int rope_dims,
+                                float scale, int window, int n_sink, attn_dtype_t dtype, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_static - attn_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart to this entry point: it exists for
  * callers that are not allowed to call cudaMalloc (or anything that does) when
@@ -224,6 +250,16 @@ ATTN_API int attn_decode_static(const void* q, const void* kcache, const void* v
  * an error.
  */
 ATTN_API int attn_device_status(void* stream);
+
+/*
+ * attn_check_wait_timeout - exercise the failure path of the bounded device
+ * waits: launches one warp that waits on a barrier nothing will ever complete.
+ * The wait gives up after the current wait limit (attn_set_wait_limit_ns), sets
+ * the status word and returns, so a following attn_device_status() reports
+ * ATTN_ERR_TIMEOUT (and clears it) while the CUDA context stays usable.  No
+ * other kernel is affected; the launch itself returns ATTN_OK or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_check_wait_timeout(void* stream);
 
 /* Number of kernels this library has launched since it was loaded. */
 ATTN_API unsigned long long attn_launch_count(void);

@@ -110,3 +110,24 @@ def test_append_then_decode_matches_prefill_last_row(lib):
     torch.cuda.synchronize()
     ref = oracle.attention_prefill(q, k, v, rope_base=base)[:, S - 1]
     assert_parity(out, ref, "bf16", "append + decode")
+
+
+@pytest.mark.parametrize("B,S,n_h,n_kv,D,window,sink,dtype", [
+    (1, 700, 4, 2, 128, 256, 4, "bf16"),    # window of 2 key tiles, 4 sinks (tensor cores)
+    (2, 520, 2, 1, 64, 300, 0, "bf16"),     # unaligned window, no sinks: rows whose first tile is all masked
+    (1, 400, 2, 2, 128, 1000, 4, "bf16"),   # window longer than the prompt: plain causal
+    (1, 333, 2, 2, 96, 100, 7, "bf16"),     # CUDA-core path
+    (1, 90, 2, 2, 16, 20, 3, "f32"),
+])
+def test_sliding_window_with_sinks(lib, B, S, n_h, n_kv, D, window, sink, dtype):
+    cfg = dict(B=B, S=S, n_h=n_h, n_kv=n_kv, D_h=D, dtype=dtype)
+    q, k, v = workloads.prefill_inputs(cfg, seed=window + sink)
+    out, _, lse = lib.prefill_window(q.to(DEV), k.to(DEV), v.to(DEV), window=window, n_sink=sink, rope_base=1e4,
+                                     lse=True)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.attention_prefill(q, k, v, rope_base=1e4, window=window, n_sink=sink, return_lse=True)
+    if dtype == "f32":
+        assert np.max(np.abs(to_np(out) - ref)) <= 1e-4
+    else:
+        assert_parity(out, ref, "bf16", f"window {window} sinks {sink}")
+        assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS

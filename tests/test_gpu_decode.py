@@ -143,3 +143,30 @@ def test_rows_past_seqlens_are_never_used(lib, name):
     assert torch.isfinite(out).all()
     ref, _ = oracle_decode(cfg, q, kc, vc, sl)
     assert_parity(out, ref, "bf16", f"{name} with NaN past seqlens")
+
+
+@pytest.mark.parametrize("name,window,sink", [
+    ("gqa_decode", 1000, 4),
+    ("gqa_decode", 300, 0),
+    ("mla_decode", 500, 4),
+])
+def test_decode_sliding_window_with_sinks(lib, name, window, sink):
+    # "Transformer 与 LLM" slide 07: keep a window of recent keys plus a few sink tokens
+    if name == "gqa_decode":
+        cfg = workloads.config(name, B=4, max_len=3000, len_lo=1, len_hi=3000)
+    else:
+        cfg = workloads.config(name, B=2, max_len=1500, len_lo=1, len_hi=1500)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=window)
+    sl[0] = 2
+    sl[-1] = cfg["max_len"]
+    kc_d = kc.to(DEV)
+    vc_d = kc_d[..., :cfg["D_v"]] if cfg.get("v_aliases_k") else vc.to(DEV)
+    out, lse = lib.decode_window(q.to(DEV), kc_d, vc_d, sl.to(DEV), window=window, n_sink=sink,
+                                 rope_base=cfg["rope_base"], rope_offset=cfg["rope_offset"],
+                                 rope_dims=cfg["rope_dims"], scale=cfg["scale"], lse=True)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.attention_decode(q, kc, vc, sl.numpy(), rope_base=cfg["rope_base"],
+                                           rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"],
+                                           scale=cfg["scale"], window=window, n_sink=sink)
+    assert_parity(out, ref, "bf16", f"{name} window {window}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS

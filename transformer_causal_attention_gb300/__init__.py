@@ -9,10 +9,13 @@ from ._binding import (  # noqa: F401
     ATTN_F32,
     AttnError,
     LIB_PATH,
+    check_wait_timeout,
     decode,
+    decode_window,
     decode_workspace_size,
     kv_append,
     prefill_chunk,
+    prefill_window,
     device_status,
     launch_count,
     load,

@@ -27,15 +27,19 @@ _vp, _i, _f, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c
 SIGNATURES = [
     ("attn_strerror", ctypes.c_char_p, [_i]),
     ("attn_prefill", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
+    ("attn_prefill_window", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _i, _vp]),
     ("attn_rope", _i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     ("attn_prefill_chunk", _i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
     ("attn_kv_append", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     ("attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i, _i, _i]),
     ("attn_decode", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
                          _vp, _sz, _vp]),
+    ("attn_decode_window", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
+                                _i, _i, _vp, _sz, _vp]),
     ("attn_decode_static", _i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i,
                                 _vp]),
     ("attn_device_status", _i, [_vp]),
+    ("attn_check_wait_timeout", _i, [_vp]),
     ("attn_launch_count", _u64, []),
     ("attn_set_wait_limit_ns", None, [_u64]),
 ]
@@ -138,6 +142,29 @@ def prefill(q, k, v, *, rope_base: float = 0.0, scale: float = 0.0, causal: bool
     return out, (k_rot if rope_base > 0 else None), lse_t
 
 
+def prefill_window(q, k, v, *, window: int, n_sink: int = 0, rope_base: float = 0.0, scale: float = 0.0,
+                   out=None, k_rot=None, lse: bool = False, stream=None):
+    """Causal sliding-window attention with attention sinks via attn_prefill_window.
+
+    Same tensors as prefill(); a query at position m sees keys n <= m with
+    m - n < window or n < n_sink.  Returns (out, k_rot or None, lse or None).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name)
+    B, S, n_h, D = q.shape
+    n_kv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if rope_base > 0 and k_rot is None:
+        k_rot = torch.empty_like(k)
+    lse_t = torch.empty((B, n_h, S), dtype=torch.float32, device=q.device) if lse else None
+    rc = _lib().attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(k_rot) if rope_base > 0 else None,
+                                    _ptr(lse_t), B, S, n_h, n_kv, D, float(rope_base), float(scale), int(window),
+                                    int(n_sink), _dtype_code(q), _stream_ptr(stream))
+    _check(rc, "attn_prefill_window")
+    return out, (k_rot if rope_base > 0 else None), lse_t
+
+
 def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = None, pos_offset: int = 0,
          out=None, stream=None):
     """RoPE of x [B,S,n_heads,D] at positions pos_offset + s via attn_rope (out may be x)."""
@@ -213,7 +240,7 @@ def decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len, dtype=torch.bfloat16
 
 def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: int = 0,
            rope_dims: int | None = None, scale: float = 0.0, out=None, lse: bool = False, workspace=None,
-           stream=None):
+           stream=None, _window=None):
     """One new token per sequence against its KV cache via attn_decode.
 
     q [B,n_h,D_qk] (un-rotated), kcache [B,L,n_kv,D_qk] (rotated keys), vcache
@@ -243,17 +270,32 @@ def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: i
     need = decode_workspace_size(B, n_h, n_kv, D_qk, D_v, L, q.dtype)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    rc = _lib().attn_decode(_ptr(q), _ptr(kcache), vcache.data_ptr(), ldv, _ptr(seqlens), _ptr(out), _ptr(lse_t),
-                            B, n_h, n_kv, D_qk, D_v, L, float(rope_base), rope_offset, rope_dims, float(scale),
-                            _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                            _stream_ptr(stream))
-    _check(rc, "attn_decode")
+    common = (_ptr(q), _ptr(kcache), vcache.data_ptr(), ldv, _ptr(seqlens), _ptr(out), _ptr(lse_t), B, n_h, n_kv,
+              D_qk, D_v, L, float(rope_base), rope_offset, rope_dims, float(scale))
+    tail = (_dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if _window is None:
+        _check(_lib().attn_decode(*common, *tail), "attn_decode")
+    else:
+        _check(_lib().attn_decode_window(*common, int(_window[0]), int(_window[1]), *tail), "attn_decode_window")
     return out, lse_t
+
+
+def decode_window(q, kcache, vcache, seqlens, *, window: int, n_sink: int = 0, rope_base: float = 0.0,
+                  rope_offset: int = 0, rope_dims: int | None = None, scale: float = 0.0, out=None,
+                  lse: bool = False, workspace=None, stream=None):
+    """decode() with a sliding window of `window` keys plus `n_sink` sink keys (attn_decode_window)."""
+    return decode(q, kcache, vcache, seqlens, rope_base=rope_base, rope_offset=rope_offset, rope_dims=rope_dims,
+                  scale=scale, out=out, lse=lse, workspace=workspace, stream=stream, _window=(window, n_sink))
 
 
 def device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the library's device status code."""
     return _lib().attn_device_status(_stream_ptr(stream))
+
+
+def check_wait_timeout(stream=None) -> None:
+    """Run the library's bounded-wait failure check (see attn_check_wait_timeout)."""
+    _check(_lib().attn_check_wait_timeout(_stream_ptr(stream)), "attn_check_wait_timeout")
 
 
 def launch_count() -> int:

@@ -135,6 +135,21 @@ int finish(cudaError_t e, int launches) {
 
 const float kLog2e = 1.4426950408889634f;
 
+// One warp waits on a barrier that nothing arrives on; the bounded wait gives
+// up after limit_ns and records STATUS_TIMEOUT.
+__global__ void wait_timeout_check_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const WaitCtl w{&abort_flag, status, limit_ns};
+  mbar_wait(&bar, 0, w);
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -174,9 +189,35 @@ int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D, i
   return finish(e, launches);
 }
 
+namespace attn {
+namespace {
+int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
+                 int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, int window, int n_sink,
+                 attn_dtype_t dtype, void* stream);
+}  // namespace
+}  // namespace attn
+
 int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
                  int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, attn_dtype_t dtype,
                  void* stream) {
+  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, rope_base, scale, causal, 0, 0, dtype, stream);
+}
+
+int attn_prefill_window(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B,
+                        int S, int n_h, int n_kv, int D_h, float rope_base, float scale, int window, int n_sink,
+                        attn_dtype_t dtype, void* stream) {
+  if (window <= 0 || n_sink < 0) return ATTN_ERR_ARG;
+  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, rope_base, scale, 1, window, n_sink, dtype,
+                      stream);
+}
+
+}  // extern "C"
+
+namespace attn {
+namespace {
+int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
+                 int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, int window, int n_sink,
+                 attn_dtype_t dtype, void* stream) {
   if (!q || !k || !v || !out) return ATTN_ERR_ARG;
   if (B <= 0 || S <= 0 || n_h <= 0 || n_kv <= 0 || D_h <= 0 || n_h % n_kv) return ATTN_ERR_ARG;
   if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
@@ -205,7 +246,7 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k
     if (e != cudaSuccess) return finish(e, launches);
   }
   PrefillArgs pa{q, rope ? k_rot : k, v, out, lse, B, S, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
-                 g_wait_limit_ns.load(), S, 0, S};
+                 g_wait_limit_ns.load(), S, 0, S, window, n_sink};
   if (prefill_tc_supported(D_h, bf16)) {
     CUtensorMap maps[3];
     if (!make_bshd_map(&maps[0], q, B, S, n_h, D_h) || !make_bshd_map(&maps[1], pa.k, B, S, n_kv, D_h) ||
@@ -217,6 +258,11 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k
   }
   return finish(e, launches);
 }
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
 
 int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, void* out, float* lse, int B, int S_q,
                        int q_offset, int max_len, int n_h, int n_kv, int D_h, float rope_base, float scale,
@@ -294,10 +340,41 @@ size_t attn_decode_workspace_size(int B, int n_h, int n_kv, int D_qk, int D_v, i
   return o_bytes + ((slots * sizeof(float) + 255) & ~size_t(255));
 }
 
+namespace attn {
+namespace {
+int decode_impl(const void* q, const void* kcache, const void* vcache, int v_token_stride, const int* seqlens,
+                void* out, float* lse, int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, float rope_base,
+                int rope_offset, int rope_dims, float scale, int window, int n_sink, attn_dtype_t dtype,
+                void* workspace, size_t workspace_bytes, void* stream);
+}  // namespace
+}  // namespace attn
+
 int attn_decode(const void* q, const void* kcache, const void* vcache, int v_token_stride, const int* seqlens,
                 void* out, float* lse, int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, float rope_base,
                 int rope_offset, int rope_dims, float scale, attn_dtype_t dtype, void* workspace,
                 size_t workspace_bytes, void* stream) {
+  return decode_impl(q, kcache, vcache, v_token_stride, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
+                     rope_base, rope_offset, rope_dims, scale, 0, 0, dtype, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_window(const void* q, const void* kcache, const void* vcache, int v_token_stride, const int* seqlens,
+                       void* out, float* lse, int B, int n_h, int n_kv, int D_qk, int D_v, int max_len,
+                       float rope_base, int rope_offset, int rope_dims, float scale, int window, int n_sink,
+                       attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (window <= 0 || n_sink < 0) return ATTN_ERR_ARG;
+  return decode_impl(q, kcache, vcache, v_token_stride, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
+                     rope_base, rope_offset, rope_dims, scale, window, n_sink, dtype, workspace, workspace_bytes,
+                     stream);
+}
+
+}  // extern "C"
+
+namespace attn {
+namespace {
+int decode_impl(const void* q, const void* kcache, const void* vcache, int v_token_stride, const int* seqlens,
+                void* out, float* lse, int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, float rope_base,
+                int rope_offset, int rope_dims, float scale, int window, int n_sink, attn_dtype_t dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !kcache || !vcache || !seqlens || !out || !workspace) return ATTN_ERR_ARG;
   if (B <= 0 || n_h <= 0 || n_kv <= 0 || n_h % n_kv || D_qk <= 0 || D_v <= 0 || max_len <= 0) return ATTN_ERR_ARG;
   if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
@@ -329,16 +406,17 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, int v_tok
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            ((slots * D_v * sizeof(float) + 255) & ~size_t(255)));
-  const bool use_mla = mla_shape(B, n_h, n_kv, D_qk, D_v, dtype) &&
+  const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, dtype) &&
                        decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, dtype == ATTN_BF16) &&
-                       (!rope || (rope_offset % 8 == 0 && rope_dims % 8 == 0));
+                       (!rope || (rope_offset % 8 == 0 && rope_dims % 8 == 0 && rope_offset >= 384));
   if (use_mla) {
     ns = decode_mla_pairs(dev.sms);  // the kernel runs 2 CTAs per pair
     chunk = 0;
   }
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_qk));
   DecodeArgs da{q, kcache, vcache, ldv, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
-                rope ? rope_offset : 0, sc * kLog2e, ws_o, ws_lse, ns, chunk, dev.status, g_wait_limit_ns.load()};
+                rope ? rope_offset : 0, sc * kLog2e, ws_o, ws_lse, ns, chunk, dev.status, g_wait_limit_ns.load(),
+                window, n_sink};
   int launches = 0;
   const bool bf16 = dtype == ATTN_BF16;
   const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0);
@@ -351,14 +429,14 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, int v_tok
         !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, 32))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);
-  } else if (decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
+  } else if (window == 0 && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
     // K and V stream through shared memory in 64-key tiles
     CUtensorMap maps[2];
     const unsigned long long ks = static_cast<unsigned long long>(D_qk) * 2;
     const unsigned long long vs = static_cast<unsigned long long>(ldv) * 2;
-    if (!make_map4(&maps[0], kcache, D_qk, n_kv, max_len, B, ks, ks * n_kv, ks * n_kv * max_len, 64) ||
+    if (!make_map4(&maps[0], kcache, D_qk, n_kv, max_len, B, ks, ks * n_kv, ks * n_kv * max_len, kStreamTileKeys) ||
         !make_map4(&maps[1], vcache, D_v, n_kv, max_len, B, static_cast<unsigned long long>(D_v) * 2, vs,
-                   vs * max_len, 64))
+                   vs * max_len, kStreamTileKeys))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_stream(da, rf, maps, dev.sms, st, &launches);
   } else {
@@ -366,6 +444,11 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, int v_tok
   }
   return finish(e, launches);
 }
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
 
 // ---------------------------------------------------------------------------
 // Decode with library-owned scratch, for callers that cannot allocate.
@@ -428,6 +511,13 @@ int attn_device_status(void* stream) {
   const unsigned int zero = 0;
   if (cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
   return (s & STATUS_TIMEOUT) ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+}
+
+int attn_check_wait_timeout(void* stream) {
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev.status, g_wait_limit_ns.load());
+  return finish(cudaGetLastError(), 1);
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(); }

@@ -65,9 +65,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a, Ro
   const int h0 = g * G + (blockIdx.y % n_hg) * HG;
   const int b = blockIdx.z;
   const int L = min(max(a.seqlens[b], 1), a.max_len);
-  const int start = split * a.chunk;
-  if (start >= L) return;  // the combine pass never reads this chunk
-  const int end = min(L, start + a.chunk);
+  const int c_lo = split * a.chunk, c_hi = min(L, c_lo + a.chunk);
+  int vlo[2], vhi[2];
+  const int nr = decode_visible(L, a.window, a.n_sink, vlo, vhi);
+  bool any = false;
+  for (int r = 0; r < nr; ++r) any |= max(c_lo, vlo[r]) < min(c_hi, vhi[r]);
+  if (!any) return;  // the combine pass never reads this chunk
   const int pos = L - 1;
 
   // rotated, pre-scaled queries of the HG heads
@@ -120,7 +123,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a, Ro
 
   // A warp takes 2*NB consecutive keys per step (NB per half-warp); the trip
   // count is uniform across the warp so the full-mask shuffles are legal.
+  // The chunk's keys are walked as (at most two) visible ranges.
   const int warp = threadIdx.x >> 5;
+  for (int r = 0; r < nr; ++r) {
+  const int start = max(c_lo, vlo[r]), end = min(c_hi, vhi[r]);
   for (int base = start + warp * 2 * NB; base < end; base += (kThreads / 32) * 2 * NB) {
     const int key0 = base + (hw & 1) * NB;
     Raw8<T> kr[NB][NQC], vr[NB][NVC];
@@ -197,6 +203,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a, Ro
     }
   }
 
+  }  // visible ranges
+
   // merge the 16 half-warps
 #pragma unroll
   for (int i = 0; i < HG; ++i) {
@@ -237,14 +245,22 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a) {
   const int L = min(max(a.seqlens[b], 1), a.max_len);
   const int ns = (L + a.chunk - 1) / a.chunk;
   const float* lse = a.ws_lse + static_cast<long long>(bh) * a.n_split;
+  int vlo[2], vhi[2];
+  const int nr = decode_visible(L, a.window, a.n_sink, vlo, vhi);
+  auto written = [&](int j) {  // chunk j holds a visible key, so its partial was written
+    bool any = false;
+    for (int r = 0; r < nr; ++r) any |= max(j * a.chunk, vlo[r]) < min(min(L, (j + 1) * a.chunk), vhi[r]);
+    return any;
+  };
   if (threadIdx.x < 32) {
     float M = -INFINITY;
-    for (int j = threadIdx.x; j < ns; j += 32) M = fmaxf(M, lse[j]);
+    for (int j = threadIdx.x; j < ns; j += 32)
+      if (written(j)) M = fmaxf(M, lse[j]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float den = 0.f;
     for (int j = threadIdx.x; j < ns; j += 32) {
-      const float w = exp2f(lse[j] - M);
+      const float w = written(j) ? exp2f(lse[j] - M) : 0.f;
       w_s[j] = w;
       den += w;
     }
@@ -261,7 +277,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a) {
   T* out = static_cast<T*>(a.out) + static_cast<long long>(bh) * a.D_v;
   for (int d = threadIdx.x; d < a.D_v; d += blockDim.x) {
     float acc = 0.f;
-    for (int j = 0; j < ns; ++j) acc = fmaf(w_s[j], po[static_cast<long long>(j) * a.D_v + d], acc);
+    for (int j = 0; j < ns; ++j)
+      if (w_s[j] != 0.f) acc = fmaf(w_s[j], po[static_cast<long long>(j) * a.D_v + d], acc);
     out[d] = from_f32<T>(acc * inv);
   }
   if (a.lse != nullptr && threadIdx.x == 0) a.lse[bh] = (stat[0] + log2f(stat[1])) * 0.69314718055994530942f;

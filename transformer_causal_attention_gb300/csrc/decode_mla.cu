@@ -12,9 +12,11 @@
 // pair walk the same keys, each computes the full score tile S = Q C^T (M = 128
 // heads, N = 32 keys, K = 576) and its own softmax, and each accumulates half of
 // the value dims (O_half += P V_half, M = 128, N = 256, K = 32).  The pair
-// reads every cache row from L2 twice but from HBM once.  Shared memory holds
-// the whole 128 x 576 query (144 KB) and a 2-stage ring of 32-key cache tiles
-// (36 KB each), all loaded by TMA with 128-byte swizzle.
+// reads every cache row from L2 twice but from HBM once.  The query is the
+// MMA's A operand: its first 384 dims sit in the TMEM columns left free by S and
+// O_half (bf16 pairs, written by the softmax warps), the last 192 dims in shared
+// memory (48 KB), which leaves room for a 4-stage ring of 32-key cache tiles
+// (36 KB each), loaded by TMA with 128-byte swizzle.
 // Keys of all sequences, laid end to end, are split evenly over the pairs
 // (a pair's range may cross sequence boundaries), so every pair does the same
 // work; each (pair, sequence) piece writes one normalised partial, merged per
@@ -35,26 +37,32 @@ constexpr int DQK = 576;         // latent + rotary dims
 constexpr int DV = 512;          // value dims
 constexpr int DVH = 256;         // value dims per CTA of a pair
 constexpr int BK = 32;           // keys per tile (MMA N of the score tile)
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kThreads = 256;
 constexpr int kBlocks = DQK / 64;                  // 9 column blocks of 64 dims
+constexpr int kQTmemDims = 384;                    // query dims [0, 384) live in TMEM (A operand)
+constexpr int kQSmemBlocks = (DQK - kQTmemDims) / 64;  // dims [384, 576) in shared memory: 3 blocks
 constexpr int kQBlockBytes = NH * 128;             // 16 KB
-constexpr int kQBytes = kBlocks * kQBlockBytes;    // 144 KB
+constexpr int kQSmemBytes = kQSmemBlocks * kQBlockBytes;  // 48 KB
 constexpr int kKBlockBytes = BK * 128;             // 4 KB
 constexpr int kTileBytes = kBlocks * kKBlockBytes; // 36 KB
 constexpr int kMaxB = 1024;
 constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kQBytes;
+constexpr int kKOff = kQOff + kQSmemBytes;
 constexpr int kPrefOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kPrefOff + (kMaxB + 1) * 4 + 60;
-constexpr int kSmemBytes = kBarOff + 128 + 1024;
-// S/P buffer b occupies TMEM columns [32 b, 32 b + 32)
+constexpr int kSmemBytes = kBarOff + 160 + 1024;
+// TMEM columns: S/P buffer b at [32 b, 32 b + 32), O_half at [64, 320), Q dims [0, 384) at [320, 512)
 __device__ __forceinline__ uint32_t s_col(uint32_t b) { return b * 32u; }
-constexpr uint32_t kOCol = 256u;
+constexpr uint32_t kOCol = 64u;
+constexpr uint32_t kQCol = 320u;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(NH, BK, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(NH, DVH, true);
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kPrefetchTiles = 8;  // tiles requested into L2 ahead of the shared-memory loads
+#ifndef ATTN_MLA_PREFETCH_TILES
+#define ATTN_MLA_PREFETCH_TILES 8
+#endif
+constexpr int kPrefetchTiles = ATTN_MLA_PREFETCH_TILES;  // tiles requested into L2 ahead of the smem loads
 
 struct Bars {
   uint64_t q_full, q_ready, q_empty;
@@ -201,17 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sb, lo, hi;
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
         if (!mbar_wait(&bars->q_empty, (n & 1) ^ 1, wc)) goto producer_done;
-        mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-        for (int blk = 0; blk < kBlocks; ++blk)
-          tma_load_3d(smem + kQOff + blk * kQBlockBytes, &tm_q, &bars->q_full, blk * 64, 0, sb);
+        mbar_arrive_expect_tx(&bars->q_full, kQSmemBytes);
+        for (int blk = 0; blk < kQSmemBlocks; ++blk)
+          tma_load_3d(smem + kQOff + blk * kQBlockBytes, &tm_q, &bars->q_full, kQTmemDims + blk * 64, 0, sb);
         q_issued = n + 1;
         // the 2-stage shared-memory ring is too shallow to cover HBM latency on its
         // own: keep kPrefetchTiles tiles ahead of the loads on their way into L2
-        for (int k0 = lo; k0 < hi && k0 < lo + kPrefetchTiles * BK; k0 += BK)
-          for (int blk = 0; blk < kBlocks; ++blk) tma_prefetch_l2_3d(&tm_c, blk * 64, k0, sb);
+        if (half == 0)  // the other CTA of the pair reads the same tiles
+          for (int k0 = lo; k0 < hi && k0 < lo + kPrefetchTiles * BK; k0 += BK)
+            for (int blk = 0; blk < kBlocks; ++blk) tma_prefetch_l2_3d(&tm_c, blk * 64, k0, sb);
         for (int k0 = lo; k0 < hi; k0 += BK) {
           const int kp = k0 + kPrefetchTiles * BK;
-          if (kp < hi)
+          if (half == 0 && kp < hi)
             for (int blk = 0; blk < kBlocks; ++blk) tma_prefetch_l2_3d(&tm_c, blk * 64, kp, sb);
           if (!mbar_wait(&bars->kv_empty[st], ph ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->kv_full[st], kTileBytes);
@@ -237,17 +246,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       PieceIter it;
       it.init(prefix, a.B, k_begin, k_end);
       const uint32_t q_addr = smem_u32(smem + kQOff);
-      uint32_t st = 0, ph = 0, pph[2] = {0u, 0u};
+      uint32_t st = 0, ph = 0, pph = 0u;  // bit b: phase of p_full[b] (bit masks keep it in registers)
       int sb, lo, hi;
       uint32_t tile = 0;  // tiles issued so far (all pieces)
       auto issue_qk = [&](uint32_t stage, uint32_t sbuf) {
         const uint32_t kaddr = smem_u32(smem + kKOff + stage * kTileBytes);
 #pragma unroll 4
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * kQBlockBytes + (kk & 3) * 32;
+        for (int kk = 0; kk < kQTmemDims / 16; ++kk) {  // A = query dims [16 kk, 16 kk + 16) from TMEM
+          const uint32_t ko = (kk >> 2) * kKBlockBytes + (kk & 3) * 32;
+          mma_ts(tmem + s_col(sbuf), tmem + kQCol + kk * 8, sdesc_sw128(kaddr + ko, 16, 1024), kIdescQK,
+                 kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = kQTmemDims / 16; kk < DQK / 16; ++kk) {  // A from shared memory
+          const int kq = kk - kQTmemDims / 16;
+          const uint32_t qo = (kq >> 2) * kQBlockBytes + (kq & 3) * 32;
           const uint32_t ko = (kk >> 2) * kKBlockBytes + (kk & 3) * 32;
           mma_ss(tmem + s_col(sbuf), sdesc_sw128(q_addr + qo, 16, 1024), sdesc_sw128(kaddr + ko, 16, 1024),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+                 kIdescQK, 1u);
         }
       };
       auto issue_pv = [&](uint32_t stage, uint32_t sbuf, bool accumulate) {
@@ -260,29 +276,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
         const int nt = (hi - lo + BK - 1) / BK;
         if (!mbar_wait(&bars->q_ready, n & 1, wc)) goto mma_done;
-        uint32_t prev_stage = 0, prev_sbuf = 0;
-        for (int j = 0; j <= nt; ++j) {
-          if (j < nt) {
-            if (!mbar_wait(&bars->kv_full[st], ph, wc)) goto mma_done;
+        // Tile j's stage is released by the commit after its P V, so P V(j) must
+        // not wait behind the next tile's load: QK(j+1) goes first only when that
+        // tile is already resident, otherwise P V(j) is issued first.
+        uint32_t cur_stage = st, cur_sbuf = tile & 1;
+        if (!mbar_wait(&bars->kv_full[st], ph, wc)) goto mma_done;
+        tc_fence_after();
+        issue_qk(st, cur_sbuf);
+        mma_commit(&bars->s_full[cur_sbuf]);
+        if (nt == 1) mma_commit(&bars->q_empty);
+        ++tile;
+        if (++st == kStages) { st = 0; ph ^= 1; }
+        for (int j = 0; j < nt; ++j) {
+          bool next_issued = false;
+          const uint32_t nstage = st, nsbuf = tile & 1;
+          if (j + 1 < nt && mbar_try_wait(&bars->kv_full[st], ph)) {
             tc_fence_after();
-            const uint32_t sbuf = tile & 1;
-            issue_qk(st, sbuf);
-            mma_commit(&bars->s_full[sbuf]);
-            if (j == nt - 1) mma_commit(&bars->q_empty);  // every MMA reading this query is issued
+            issue_qk(st, nsbuf);
+            mma_commit(&bars->s_full[nsbuf]);
+            if (j + 1 == nt - 1) mma_commit(&bars->q_empty);  // every MMA reading this query is issued
+            next_issued = true;
           }
-          if (j >= 1) {
-            // P of the previous tile is ready: O_half += P V_half
-            if (!mbar_wait(&bars->p_full[prev_sbuf], pph[prev_sbuf], wc)) goto mma_done;
-            pph[prev_sbuf] ^= 1;
-            if (j == 1 && !mbar_wait(&bars->o_empty, (n & 1) ^ 1, wc)) goto mma_done;
-            tc_fence_after();
-            issue_pv(prev_stage, prev_sbuf, j > 1);
-            mma_commit(&bars->pv_done);
-            mma_commit(&bars->kv_empty[prev_stage]);
-          }
-          if (j < nt) {
-            prev_stage = st;
-            prev_sbuf = tile & 1;
+          if (!mbar_wait(&bars->p_full[cur_sbuf], (pph >> cur_sbuf) & 1u, wc)) goto mma_done;
+          pph ^= 1u << cur_sbuf;
+          if (j == 0 && !mbar_wait(&bars->o_empty, (n & 1) ^ 1, wc)) goto mma_done;
+          tc_fence_after();
+          issue_pv(cur_stage, cur_sbuf, j > 0);
+          mma_commit(&bars->pv_done);
+          mma_commit(&bars->kv_empty[cur_stage]);
+          if (j + 1 < nt) {
+            if (!next_issued) {
+              if (!mbar_wait(&bars->kv_full[st], ph, wc)) goto mma_done;
+              tc_fence_after();
+              issue_qk(st, nsbuf);
+              mma_commit(&bars->s_full[nsbuf]);
+              if (j + 1 == nt - 1) mma_commit(&bars->q_empty);
+            }
+            cur_stage = nstage;
+            cur_sbuf = nsbuf;
             ++tile;
             if (++st == kStages) { st = 0; ph ^= 1; }
           }
@@ -300,22 +331,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     PieceIter it;
     it.init(prefix, a.B, k_begin, k_end);
-    uint32_t sph[2] = {0u, 0u}, pvph = 0, st = 0, tile = 0;
+    uint32_t sph = 0u, pvph = 0, st = 0, tile = 0;  // sph bit b: phase of s_full[b]
     int sb, lo, hi;
     for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
       const int nt = (hi - lo + BK - 1) / BK;
       const int L = prefix[sb + 1] - prefix[sb];
+      // query dims [0, 384) of head h -> TMEM columns [kQCol, kQCol + 192) as bf16 pairs (the
+      // A-operand layout: row = lane, two consecutive k per 32-bit column); the previous
+      // piece's QK MMAs must have finished reading them
+      if (!warp_wait(&bars->q_empty, (n & 1) ^ 1, wc)) break;
+      tc_fence_after();
+      {
+        const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                           (static_cast<long long>(sb) * a.n_h + h) * DQK);
+#pragma unroll 1
+        for (int c = 0; c < kQTmemDims / 64; ++c) {  // 32 columns = 64 dims per store
+          uint32_t r[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 u = qrow[c * 8 + e];
+            r[4 * e] = u.x;
+            r[4 * e + 1] = u.y;
+            r[4 * e + 2] = u.z;
+            r[4 * e + 3] = u.w;
+          }
+          tmem_st32(tmem + lane_off + kQCol + c * 32, r);
+        }
+        tmem_wait_st();
+      }
       if (!warp_wait(&bars->q_full, n & 1, wc)) break;
       if (f.n_pairs) {
-        // rotate this head's dims [rope_offset, rope_offset + rope_dims) at the new token's position
+        // rotate this head's dims [rope_offset, rope_offset + rope_dims) (all in the shared-memory
+        // part) at the new token's position
         uint8_t* row = smem + kQOff + h * 128;
-        for (int c = a.rope_offset / 8; c < (a.rope_offset + 2 * f.n_pairs) / 8; ++c) {
+        for (int c = (a.rope_offset - kQTmemDims) / 8; c < (a.rope_offset + 2 * f.n_pairs - kQTmemDims) / 8; ++c) {
           uint4* ptr = reinterpret_cast<uint4*>(row + (c >> 3) * kQBlockBytes + (((c & 7) ^ (h & 7)) << 4));
           float x[8];
           bf16x8_to_f32(*ptr, x);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int rp = (c * 8 + 2 * e - a.rope_offset) / 2;
+            const int rp = (kQTmemDims + c * 8 + 2 * e - a.rope_offset) / 2;
             float sn, cs;
             rope_sincos(L - 1, f.hi[rp], f.lo[rp], &sn, &cs);
             rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
@@ -324,14 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
       }
+      tc_fence_before();
       mbar_arrive(&bars->q_ready);
 
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const uint32_t sbuf = tile & 1;
-        if (!warp_wait(&bars->s_full[sbuf], sph[sbuf], wc)) { ok = false; break; }
-        sph[sbuf] ^= 1;
+        if (!warp_wait(&bars->s_full[sbuf], (sph >> sbuf) & 1u, wc)) { ok = false; break; }
+        sph ^= 1u << sbuf;
         tc_fence_after();
         uint32_t sr[BK];
         tmem_ld32(tmem + lane_off + s_col(sbuf), sr);

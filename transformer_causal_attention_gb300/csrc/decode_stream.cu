@@ -4,9 +4,11 @@
 // Decode reads each cached key/value row once and is bound by HBM bandwidth
 // ("Transformer架构完全深度解析" §9).  To keep enough bytes in flight the kernel
 // is persistent (one CTA per SM) and splits roles:
-//   warp 0      TMA producer: for every work unit (sequence b, KV head g, group
-//               of 4 query heads, chunk of keys) it streams 64-key K and V tiles
-//               into a 5-stage ring (32 KB per stage, 128-byte swizzle);
+//   warp 0      TMA producer: for every work unit (sequence b, chunk of keys,
+//               group of 4 query heads, KV head g) it first asks for the whole
+//               unit to be pulled into L2 (many DRAM reads in flight, each line
+//               used shortly after), then streams 64-key K and V tiles into a
+//               5-stage ring (32 KB per stage, 128-byte swizzle);
 //   warps 1-8   consumers: each half-warp scores 4 keys of a tile against the 4
 //               query heads (lane = 8 dims, packed fp32x2 FMAs), reduces the 16
 //               partial dot products with a reduce-scatter butterfly (15
@@ -26,7 +28,8 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HG = 4;                 // query heads per unit
-constexpr int BK = 64;                // keys per tile
+constexpr int BK = kStreamTileKeys;   // keys per tile
+static_assert(BK == 64, "16 half-warps x 4 keys");
 constexpr int NB = 4;                 // keys per half-warp per tile (16 half-warps x 4 = BK)
 constexpr int kStages = 5;
 constexpr int kConsumerWarps = 8;
@@ -127,17 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         Unit w;
         if (!unit_at(u, a, w)) continue;
-        // pull the next unit of this CTA into L2 while this one streams through shared memory
-        Unit nx;
-        for (int u2 = u + gridDim.x; u2 < n_units; u2 += gridDim.x) {
-          if (!unit_at(u2, a, nx)) continue;
-          for (int k0 = nx.start; k0 < nx.end; k0 += BK)
-            for (int db = 0; db < D / 64; ++db) {
-              tma_prefetch_l2_4d(&tm_k, db * 64, nx.g, k0, nx.b);
-              tma_prefetch_l2_4d(&tm_v, db * 64, nx.g, k0, nx.b);
-            }
-          break;
-        }
+        for (int k0 = w.start; k0 < w.end; k0 += BK)
+          for (int db = 0; db < D / 64; ++db) {
+            tma_prefetch_l2_4d(&tm_k, db * 64, w.g, k0, w.b);
+            tma_prefetch_l2_4d(&tm_v, db * 64, w.g, k0, w.b);
+          }
         for (int k0 = w.start; k0 < w.end; k0 += BK) {
           if (!mbar_wait(&bars->empty[st], ph ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->full[st], kStageBytes);

@@ -24,6 +24,8 @@ struct PrefillArgs {
   int S_k;           // keys visible per sequence (keys 0 .. S_k-1)
   int q_offset;      // absolute position of query row 0 (a chunk continuing a cache)
   int kv_rows;       // rows per sequence in the K/V buffers (S for a prompt, max_len for a cache)
+  int window;        // > 0: a query at position p sees keys n with p - n < window ...
+  int n_sink;        // ... plus the first n_sink keys (attention sinks); window 0: no window
 };
 
 struct DecodeArgs {
@@ -42,7 +44,30 @@ struct DecodeArgs {
   int n_split, chunk;
   unsigned int* status;
   unsigned long long wait_limit_ns;
+  int window;  // > 0: the new token (position L-1) sees keys n with L-1-n < window, plus n < n_sink
+  int n_sink;
 };
+
+// Visible keys of a decode query at position L - 1: [0, L) without a window,
+// else [0, min(n_sink, L)) and [max(0, L - window), L).  Returns the number of
+// key ranges (1 or 2) in lo/hi.
+__host__ __device__ __forceinline__ int decode_visible(int L, int window, int n_sink, int* lo, int* hi) {
+  if (window <= 0 || L - window <= n_sink) {  // no window, or window and sinks touch: all keys
+    lo[0] = 0;
+    hi[0] = L;
+    return 1;
+  }
+  if (n_sink <= 0) {
+    lo[0] = L - window;
+    hi[0] = L;
+    return 1;
+  }
+  lo[0] = 0;
+  hi[0] = n_sink;
+  lo[1] = L - window;
+  hi[1] = L;
+  return 2;
+}
 
 struct RopeArgs {
   void* out;
@@ -79,6 +104,7 @@ bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long
 int decode_mla_pairs(int num_sms);
 cudaError_t launch_decode_mla(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, cudaStream_t st,
                               int* launches);
+constexpr int kStreamTileKeys = 64;  // keys per TMA box of the streaming GQA decode
 bool decode_stream_supported(int n_h, int n_kv, int D_qk, int D_v, bool bf16);
 cudaError_t launch_decode_stream(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
                                  cudaStream_t st, int* launches);

@@ -63,34 +63,43 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(PrefillArgs a, RopeFr
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
   float m_run = -INFINITY, l = 0.f;
-  const int n_end = a.causal ? a.q_offset + m + 1 : a.S_k;
+  const int pos = a.q_offset + m;
+  const int n_end = a.causal ? pos + 1 : a.S_k;
+  // visible keys: [0, n_end), or with a window the sinks [0, n_sink) and [pos - window + 1, n_end)
+  int win_lo = 0;
+  if (a.window > 0) win_lo = max(0, pos - a.window + 1);
+  const int sink_end = (a.window > 0 && a.n_sink < win_lo) ? a.n_sink : 0;
+  if (a.window > 0 && a.n_sink >= win_lo) win_lo = 0;  // sinks and window overlap: one range
 
-  for (int n0 = 0; n0 < n_end; n0 += 32) {
-    const int n = n0 + lane;
-    float s = -INFINITY;
-    if (n < n_end) {
-      const T* kr = kbase + n * row_stride;
-      float dot = 0.f;
-      for (int d = 0; d < D; ++d) dot = fmaf(q_s[warp][d], to_f32(kr[d]), dot);
-      s = dot;
-    }
-    const float m_new = fmaxf(m_run, warp_max(s));  // finite: lane 0 always holds a visible key
-    const float alpha = exp2f(m_run - m_new);
-    const float p = (n < n_end) ? exp2f(s - m_new) : 0.f;
-    l = l * alpha + warp_sum(p);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] *= alpha;
-    const int cnt = min(32, n_end - n0);
-    for (int j = 0; j < cnt; ++j) {
-      const float pj = __shfl_sync(0xffffffffu, p, j);
-      const T* vr = vbase + (n0 + j) * row_stride;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int d = lane + 32 * t;
-        if (d < D) acc[t] = fmaf(pj, to_f32(vr[d]), acc[t]);
+  for (int range = 0; range < 2; ++range) {
+    const int r_lo = range == 0 ? 0 : win_lo, r_hi = range == 0 ? sink_end : n_end;
+    for (int n0 = r_lo; n0 < r_hi; n0 += 32) {
+      const int n = n0 + lane;
+      float s = -INFINITY;
+      if (n < r_hi) {
+        const T* kr = kbase + n * row_stride;
+        float dot = 0.f;
+        for (int d = 0; d < D; ++d) dot = fmaf(q_s[warp][d], to_f32(kr[d]), dot);
+        s = dot;
       }
+      const float m_new = fmaxf(m_run, warp_max(s));  // finite: lane 0 always holds a visible key
+      const float alpha = exp2f(m_run - m_new);
+      const float p = (n < r_hi) ? exp2f(s - m_new) : 0.f;
+      l = l * alpha + warp_sum(p);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t] *= alpha;
+      const int cnt = min(32, r_hi - n0);
+      for (int j = 0; j < cnt; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+        const T* vr = vbase + (n0 + j) * row_stride;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int d = lane + 32 * t;
+          if (d < D) acc[t] = fmaf(pj, to_f32(vr[d]), acc[t]);
+        }
+      }
+      m_run = m_new;
     }
-    m_run = m_new;
   }
 
   T* orow = static_cast<T*>(a.out) + ((static_cast<long long>(b) * a.S + m) * a.n_h + h) * D;

@@ -63,14 +63,42 @@ struct Bars {
   int abort_flag;
 };
 
-struct Item {
-  int b, h, g, qt0, n0, n1;
+// Key tiles of one Q tile: [0, ns) (attention-sink tiles kept outside the
+// window) followed by [jl, jh] (the window up to the diagonal).  Without a
+// window ns = 0, jl = 0 and jh is the last tile at or before the diagonal.
+struct TileRange {
+  int ns, jl, jh;
+  __device__ __forceinline__ int count() const { return ns + jh - jl + 1; }
+  __device__ __forceinline__ bool has(int j) const { return j < ns || (j >= jl && j <= jh); }
+  __device__ __forceinline__ int at(int i) const { return i < ns ? i : jl + i - ns; }  // i-th tile
 };
 
-// Key tiles a causal Q tile needs: up to the tile holding its last query's position.
-__device__ __forceinline__ int causal_tiles(int qt, const PrefillArgs& a) {
-  const int last_row = min(qt * BM + BM - 1, a.S - 1);
-  return (a.q_offset + last_row) / BN + 1;
+struct Item {
+  int b, h, g, qt0;
+  TileRange r0, r1;  // the two Q tiles
+  int ns_u, n_load;  // loaded tiles: [0, ns_u) then [r0.jl, r1.jh]
+  __device__ __forceinline__ int load_at(int v) const { return v < ns_u ? v : r0.jl + v - ns_u; }
+};
+
+__device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, int n_kt) {
+  TileRange r;
+  if (!a.causal) {
+    r.ns = 0;
+    r.jl = 0;
+    r.jh = n_kt - 1;
+    return r;
+  }
+  const int first_pos = a.q_offset + qt * BM;
+  const int last_pos = a.q_offset + min(qt * BM + BM - 1, a.S - 1);
+  r.jh = last_pos / BN;
+  if (a.window > 0) {
+    r.jl = max(0, first_pos - a.window + 1) / BN;
+    r.ns = min((a.n_sink + BN - 1) / BN, r.jl);
+  } else {
+    r.jl = 0;
+    r.ns = 0;
+  }
+  return r;
 }
 
 __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n_pairs_q, int n_kt) {
@@ -82,12 +110,12 @@ __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n
   it.h = bh % a.n_h;
   it.g = it.h / (a.n_h / a.n_kv);
   it.qt0 = 2 * p;
-  if (a.causal) {
-    it.n0 = causal_tiles(it.qt0, a);
-    it.n1 = causal_tiles(it.qt0 + 1, a);
-  } else {
-    it.n0 = it.n1 = n_kt;
-  }
+  it.r0 = tile_range(it.qt0, a, n_kt);
+  it.r1 = tile_range(it.qt0 + 1, a, n_kt);
+  // tile 1's window starts no earlier and ends no earlier than tile 0's, and its
+  // sink tiles beyond tile 0's lie inside tile 0's window, so the union is:
+  it.ns_u = it.r0.ns;
+  it.n_load = it.ns_u + it.r1.jh - it.r0.jl + 1;
   return it;
 }
 
@@ -159,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, a.status, a.wait_limit_ns};
 
-  uint8_t* q_smem[2] = {smem + C::kQOff, smem + C::kQOff + C::kTileBytes};
+  // Q tile t lives at smem + kQOff + t * kTileBytes (arithmetic, not an array:
+  // runtime-indexed local arrays would live in local memory)
+  auto q_smem = [&](int t) { return smem + C::kQOff + t * C::kTileBytes; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -175,11 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars->q_empty[t], (it & 1) ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
           for (int db = 0; db < C::kDBlocks; ++db)
-            tma_load_4d(q_smem[t] + db * C::kBlockBytes, &tm_q, &bars->q_full[t], db * 64, itm.h,
+            tma_load_4d(q_smem(t) + db * C::kBlockBytes, &tm_q, &bars->q_full[t], db * 64, itm.h,
                         (itm.qt0 + t) * BM, itm.b);
           q_issued = it + 1;
         }
-        for (int j = 0; j < itm.n1; ++j) {
+        for (int v = 0; v < itm.n_load; ++v) {
+          const int j = itm.load_at(v);
           if (!mbar_wait(&bars->k_empty[kst], kph ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->k_full[kst], C::kTileBytes);
           uint8_t* kdst = smem + C::kKOff + kst * C::kTileBytes;
@@ -213,71 +244,84 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t s_col[2] = {0u, 128u};
-      const uint32_t o_col[2] = {C::kOCol0, C::kOCol0 + D};
-      uint32_t q_addr[2] = {smem_u32(q_smem[0]), smem_u32(q_smem[1])};
+      const uint32_t q_addr0 = smem_u32(q_smem(0));
       uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
-      uint32_t pph[2] = {0u, 0u};
+      uint32_t pph0 = 0u, pph1 = 0u;
       uint32_t it = 0;
       auto issue_qk = [&](int t, uint32_t stage) {
         const uint32_t kbase = smem_u32(smem + C::kKOff + stage * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_ss(tmem + s_col[t], sdesc_sw128(q_addr[t] + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                 C::kIdescQK, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + t * 128u, sdesc_sw128(q_addr0 + t * C::kTileBytes + off, 16, 1024),
+                 sdesc_sw128(kbase + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
         const uint32_t vbase = smem_u32(smem + C::kVOff + stage * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, sdesc_sw128(vbase + kk * 16 * 128, C::kBlockBytes, 1024),
-                 C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kOCol0 + t * D, tmem + t * 128u + kk * 8,
+                 sdesc_sw128(vbase + kk * 16 * 128, C::kBlockBytes, 1024), C::kIdescPV,
+                 (accumulate || kk > 0) ? 1u : 0u);
         }
       };
       for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
         const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
-        // first key tile: S_0 and S_1
+        // Loaded tile v feeds Q tile t when t's range has it.  Per loaded tile:
+        // P V of every member tile, then QK of the next loaded tile for its
+        // members (so S_t is reused only after P_t was consumed; MMAs run in order).
+        bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
         if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
-        for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
-          tc_fence_after();
-          issue_qk(t, kst);
-          mma_commit(&bars->s_full[t]);
+        {
+          const int j0 = itm.load_at(0);
+          for (int t = 0; t < 2; ++t) {
+            if (!(t ? itm.r1 : itm.r0).has(j0)) continue;
+            if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+            (t ? q_seen1 : q_seen0) = true;
+            tc_fence_after();
+            issue_qk(t, kst);
+            mma_commit(&bars->s_full[t]);
+          }
         }
         mma_commit(&bars->k_empty[kst]);
         if (++kst == C::kStages) { kst = 0; kph ^= 1; }
-        for (int j = 0; j < itm.n1; ++j) {
+        for (int v = 0; v < itm.n_load; ++v) {
+          const int j = itm.load_at(v);
+          const bool next = v + 1 < itm.n_load;
+          const int jn = next ? itm.load_at(v + 1) : -1;
           if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
-          if (j < itm.n0) {
-            if (!mbar_wait(&bars->p_full[0], pph[0], wc)) goto mma_done;
-            pph[0] ^= 1;
-            if (j == 0 && !mbar_wait(&bars->o_empty[0], (it & 1) ^ 1, wc)) goto mma_done;
-            tc_fence_after();
-            issue_pv(0, vst, j > 0);
-            if (j == itm.n0 - 1) mma_commit(&bars->o_done[0]);
-          }
-          const bool next = j + 1 < itm.n1;
-          if (next) {
-            if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
-            tc_fence_after();
-            if (j + 1 < itm.n0) {
-              issue_qk(0, kst);
-              mma_commit(&bars->s_full[0]);
+          bool k_ready = false;
+          for (int t = 0; t < 2; ++t) {
+            const TileRange& r = t ? itm.r1 : itm.r0;
+            if (r.has(j)) {
+              if (!mbar_wait(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
+              if (t) pph1 ^= 1; else pph0 ^= 1;
+              const bool seen = t ? pv_seen1 : pv_seen0;
+              if (!seen && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
+              tc_fence_after();
+              issue_pv(t, vst, seen);
+              if (t) pv_seen1 = true; else pv_seen0 = true;
+              if (j == r.jh) mma_commit(&bars->o_done[t]);
+            }
+            if (t == 1) {
+              mma_commit(&bars->v_empty[vst]);
+              if (++vst == C::kStages) { vst = 0; vph ^= 1; }
+            }
+            if (next && r.has(jn)) {
+              if (!k_ready) {
+                if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
+                k_ready = true;
+              }
+              const bool qs = t ? q_seen1 : q_seen0;
+              if (!qs && !mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+              if (t) q_seen1 = true; else q_seen0 = true;
+              tc_fence_after();
+              issue_qk(t, kst);
+              mma_commit(&bars->s_full[t]);
             }
           }
-          if (!mbar_wait(&bars->p_full[1], pph[1], wc)) goto mma_done;
-          pph[1] ^= 1;
-          if (j == 0 && !mbar_wait(&bars->o_empty[1], (it & 1) ^ 1, wc)) goto mma_done;
-          tc_fence_after();
-          issue_pv(1, vst, j > 0);
-          mma_commit(&bars->v_empty[vst]);
-          if (++vst == C::kStages) { vst = 0; vph ^= 1; }
-          if (j == itm.n1 - 1) mma_commit(&bars->o_done[1]);
           if (next) {
-            issue_qk(1, kst);
-            mma_commit(&bars->s_full[1]);
             mma_commit(&bars->k_empty[kst]);
             if (++kst == C::kStages) { kst = 0; kph ^= 1; }
           }
@@ -302,14 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
       const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
-      const int n_t = t ? itm.n1 : itm.n0;
+      const TileRange rng = t ? itm.r1 : itm.r0;
+      const int n_t = rng.count();
       const int m = qt * BM + r;  // query row
       const int pos = a.q_offset + m;  // its absolute position
       if (!warp_wait(&bars->q_full[t], it & 1, wc)) break;
       if (f.n_pairs) {
         // rotate this thread's query row in place (swizzled layout: the 16-byte
         // chunk c of row r sits at chunk c ^ (r & 7) of the row's 128-byte line)
-        uint8_t* row = q_smem[t] + r * 128;
+        uint8_t* row = q_smem(t) + r * 128;
 #pragma unroll 1
         for (int c = 0; c < D / 8; ++c) {
           uint4* p = reinterpret_cast<uint4*>(row + (c >> 3) * C::kBlockBytes + (((c & 7) ^ (r & 7)) << 4));
@@ -329,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      for (int j = 0; j < n_t; ++j) {
+      for (int i = 0; i < n_t; ++i) {
+        const int j = rng.at(i);  // key tile
         if (!warp_wait(&bars->s_full[t], sph, wc)) { ok = false; break; }
         sph ^= 1;
         tc_fence_after();
@@ -341,7 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
         const int key0 = j * BN;
-        if (a.causal && key0 + BN - 1 > a.q_offset + qt * BM) {
+        const int tile_pos0 = a.q_offset + qt * BM;  // position of the Q tile's first row
+        if (a.window > 0 && tile_pos0 + BM - 1 - key0 >= a.window && key0 + BN > a.n_sink) {
+          // some key of this tile is outside some row's window (and not a sink)
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int key = key0 + c;
+            if (key > pos || (pos - key >= a.window && key >= a.n_sink)) s[c] = -INFINITY;
+          }
+        } else if (a.causal && key0 + BN - 1 > tile_pos0) {
           // some key of this tile lies after some query of the Q tile: mask key > position
 #pragma unroll
           for (int c = 0; c < BN; ++c)
@@ -368,28 +422,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mx > m_run + kRescaleThreshold;
         float alpha = 1.f;
         if (need) {
-          if (j > 0) alpha = fast_exp2(m_run - mx);
+          if (i > 0) alpha = fast_exp2(m_run - mx);
           l_run *= alpha;
           m_run = mx;
-        }
-        // TMEM loads/stores are warp-collective: the whole warp rescales when any
-        // of its rows needs it (alpha is 1 for the others).
-        if (__any_sync(0xffffffffu, need && j > 0)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t orow[32];
-            tmem_ld32(o_addr + c * 32, orow);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
-            tmem_st32(o_addr + c * 32, orow);
-          }
         }
         // p = 2^(s * scale*log2e - m), two columns per packed fp32x2 FMA; the row
         // sum runs in 4 independent packed accumulators
         uint32_t pr[BN / 2];
         const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
-        const float2 nm2 = make_float2(-m_run, -m_run);
+        // a row whose tiles so far held no visible key keeps m = -inf: its
+        // weights are 0 (reference 0 avoids -inf - -inf)
+        const float m_ref = (m_run == -INFINITY) ? 0.f : m_run;
+        const float2 nm2 = make_float2(-m_ref, -m_ref);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
@@ -402,6 +446,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run += acc[0].x + acc[0].y;
         tmem_st32(s_addr, pr);
         tmem_st32(s_addr + 32, pr + 32);
+        // O rescale, once the scores are dead (fewer live registers).  P V(j-1)
+        // has completed (s_full of tile j was committed after it), P V(j) waits
+        // for p_full below.  TMEM loads/stores are warp-collective: the whole
+        // warp rescales when any of its rows needs it (alpha is 1 for the others).
+        if (__any_sync(0xffffffffu, need && i > 0)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(o_addr + c * 32, orow);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+            tmem_st32(o_addr + c * 32, orow);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
