@@ -41,7 +41,26 @@
 extern "C" {
 #endif
 
-typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+/*
+ * The dtype argument of every call: the element type in the low byte, with
+ * ATTN_ROPE_HALF optionally OR'd in by any call that applies RoPE.  That flag
+ * pairs dimension j of the rotated span with j + rope_dims/2 (the split-halves
+ * layout of the apply_rope code in "2.7 Transformer Decoder Block完整解析" §4)
+ * instead of (2i, 2i+1); pair j still turns by pos * rope_base^(-2j/rope_dims).
+ * Either layout is a rotation of 2-d subspaces ("Transformer架构从Attention到
+ * DecoderBlock" §8.1 allows both if training and inference agree): keys written
+ * to a cache with one pairing must be read back by calls using the same one.
+ * With the flag, each half of a rotated span must consist of whole chunks where
+ * a call asks for multiples of 8 (16 instead of 8; 4 instead of 2 for ATTN_F32).
+ * Any other bit is ATTN_ERR_ARG.
+ */
+typedef enum {
+  ATTN_F32 = 0,
+  ATTN_BF16 = 1,
+  ATTN_ROPE_HALF = 0x100,
+  ATTN_F32_ROPE_HALF = ATTN_F32 | ATTN_ROPE_HALF,
+  ATTN_BF16_ROPE_HALF = ATTN_BF16 | ATTN_ROPE_HALF
+} attn_dtype_t;
 
 enum {
   ATTN_OK = 0,
@@ -84,6 +103,38 @@ ATTN_API const char* attn_strerror(int code);
 ATTN_API int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k_rot,
                  float* lse, int B, int S, int n_h, int n_kv, int D_h, float rope_base,
                  float scale, int causal, attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_prefill_mla - prefill with separate head dims for q/k and v and RoPE on
+ * a span of the q/k dims: the non-absorbed path of Multi-head Latent Attention
+ * ("Transformer 与 LLM" slide 06).  There every head scores
+ * q . [k^C ; k^R] / sqrt(192): a 128-dim content part (the latent c^KV
+ * up-projected per head) and a 64-dim decoupled RoPE part k^R that all heads
+ * share, against values of 128 dims; the slide notes that prefill takes this
+ * path because absorbing W_UK / W_UV would cost ~3.4x the attention FLOPs.
+ * The call is that MHA-like attention for any (D_qk, D_v):
+ *
+ *   q      [B, S, n_h,  D_qk]  queries, NOT rotated.
+ *   k      [B, S, n_kv, D_qk]  keys, NOT rotated (the caller writes k^R into
+ *                              the last rope_dims dims of every head).
+ *   v      [B, S, n_kv, D_v]   values.
+ *   out    [B, S, n_h,  D_v].
+ *   k_rot  [B, S, n_kv, D_qk]  receives k with its RoPE span rotated; required
+ *                              when rope_base > 0, must not overlap k.
+ *   lse    [B, n_h, S] fp32    optional, as attn_prefill.
+ *   rope_base > 0 rotates dims [rope_offset, rope_offset + rope_dims) of q and
+ *              k at their positions with theta_i = rope_base^(-2i/rope_dims);
+ *              <= 0: no RoPE (offset and dims ignored).
+ *   scale     > 0: score multiplier; <= 0: 1/sqrt(D_qk) (1/sqrt(192) for MLA).
+ *   causal    1: mask keys n > m; 0: no mask.
+ * Tensor cores run (D_qk, D_v) = (64, 64), (128, 128) and (192, 128) in bf16;
+ * other sizes up to 256 (multiples of 8 in bf16, of 2 in fp32) run on CUDA
+ * cores.  rope_offset must be a multiple of 8 (bf16) or 2 (fp32) and
+ * rope_dims of 8 or 2 (16 or 4 with ATTN_ROPE_HALF).  Errors as attn_prefill.
+ */
+ATTN_API int attn_prefill_mla(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse,
+                              int B, int S, int n_h, int n_kv, int D_qk, int D_v, float rope_base, int rope_offset,
+                              int rope_dims, float scale, int causal, attn_dtype_t dtype, void* stream);
 
 /*
  * attn_rope - rotate dims [rope_offset, rope_offset + rope_dims) of every row

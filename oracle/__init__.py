@@ -16,6 +16,7 @@ from .attention import (  # noqa: F401
     logsumexp_rows,
     mla_absorb_query,
     mla_decode_unabsorbed,
+    mla_prefill_unabsorbed,
     mla_unabsorb_output,
     rope_cache,
     rope_frequencies,

@@ -159,14 +159,17 @@ def default_scale(D_h: int, scale: float | None) -> float:
 # --------------------------------------------------------------------------
 def attention_prefill(q, k, v, *, rope_base: float = 0.0, scale: float | None = None,
                       causal: bool = True, q_offset: int = 0, window: int = 0,
-                      n_sink: int = 0, pairing: str = "adjacent", return_lse: bool = False):
+                      n_sink: int = 0, pairing: str = "adjacent", rope_offset: int = 0,
+                      rope_dims: int | None = None, return_lse: bool = False):
     """Multi-head causal attention over a whole prompt.
 
     q [B, S_q, n_h, D_h], k [B, S_k, n_kv, D_h], v [B, S_k, n_kv, D_v] (BSHD, the
     layout the pages' code reaches after .view(batch, seq, heads, d_k)).  Query
     row m sits at position q_offset + m, key row n at position n.  RoPE is
-    applied to q and k when rope_base > 0.  Returns out [B, S_q, n_h, D_v]
-    (float64) and, on request, lse [B, n_h, S_q] (natural log).
+    applied to dims [rope_offset, rope_offset + rope_dims) of q and k (all of
+    them by default) when rope_base > 0.  The value head dim D_v may differ
+    from D_h (MLA prefill: D_h = 192, D_v = 128).  Returns out [B, S_q, n_h,
+    D_v] (float64) and, on request, lse [B, n_h, S_q] (natural log).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, S_q, n_h, D = q.shape
@@ -176,8 +179,9 @@ def attention_prefill(q, k, v, *, rope_base: float = 0.0, scale: float | None = 
     G = n_h // n_kv
     scale = default_scale(D, scale)
     if rope_base > 0:
-        q = rope_rotate(q, (q_offset + np.arange(S_q))[None, :, None], rope_base, pairing=pairing)
-        k = rope_rotate(k, np.arange(S_k)[None, :, None], rope_base, pairing=pairing)
+        q = rope_rotate(q, (q_offset + np.arange(S_q))[None, :, None], rope_base, rope_offset, rope_dims,
+                        pairing=pairing)
+        k = rope_rotate(k, np.arange(S_k)[None, :, None], rope_base, rope_offset, rope_dims, pairing=pairing)
     mask = None
     if causal or window > 0:
         mask = causal_mask(S_q, S_k, q_offset, window, n_sink)
@@ -193,7 +197,8 @@ def attention_prefill(q, k, v, *, rope_base: float = 0.0, scale: float | None = 
 
 
 def attention_prefill_rows(q, k, v, b: int, h: int, rows, *, rope_base: float = 0.0,
-                           scale: float | None = None, causal: bool = True):
+                           scale: float | None = None, causal: bool = True, rope_offset: int = 0,
+                           rope_dims: int | None = None):
     """Selected output rows of attention_prefill for one (b, h), computed one
     query at a time so that full-size problems can be sampled.  Returns
     (out [len(rows), D_v], lse [len(rows)])."""
@@ -206,8 +211,8 @@ def attention_prefill_rows(q, k, v, b: int, h: int, rows, *, rope_base: float = 
     vv = _f64(v[b, :, g, :])
     qq = _f64(q[b, rows, h, :])
     if rope_base > 0:
-        qq = rope_rotate(qq, rows, rope_base)
-        kk = rope_rotate(kk, np.arange(kk.shape[0]), rope_base)
+        qq = rope_rotate(qq, rows, rope_base, rope_offset, rope_dims)
+        kk = rope_rotate(kk, np.arange(kk.shape[0]), rope_base, rope_offset, rope_dims)
     outs, lses = [], []
     for i, m in enumerate(rows):
         n_vis = int(m) + 1 if causal else kk.shape[0]
@@ -223,14 +228,15 @@ def attention_prefill_rows(q, k, v, b: int, h: int, rows, *, rope_base: float = 
 def attention_decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0,
                      rope_offset: int = 0, rope_dims: int | None = None,
                      scale: float | None = None, window: int = 0, n_sink: int = 0,
-                     batch_index=None):
+                     pairing: str = "adjacent", batch_index=None):
     """One new query token per sequence against its cache.
 
     q [B, n_h, D_qk] un-rotated; kcache [B, L_max, n_kv, D_qk] holding rotated
     keys; vcache [B, L_max, n_kv, D_v]; seqlens[b] keys are valid and already
     include the new token, which therefore sits at position seqlens[b] - 1
     ("Transformer架构完全深度解析" §9: append, then attend).  RoPE (when
-    rope_base > 0) rotates dims [rope_offset, rope_offset + rope_dims) of q.
+    rope_base > 0) rotates dims [rope_offset, rope_offset + rope_dims) of q
+    with the given pairing (it must match the one the cache was written with).
     batch_index restricts the work to a subset of sequences.  Returns
     out [B, n_h, D_v] (rows outside batch_index stay 0) and lse [B, n_h].
     """
@@ -252,7 +258,7 @@ def attention_decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0,
         pos = L - 1
         qb = q[b]
         if rope_base > 0:
-            qb = rope_rotate(qb, np.full(n_h, pos), rope_base, rope_offset, rope_dims)
+            qb = rope_rotate(qb, np.full(n_h, pos), rope_base, rope_offset, rope_dims, pairing=pairing)
         mask = None
         if window > 0:
             mask = causal_mask(1, L, pos, window, n_sink)
@@ -300,6 +306,33 @@ def mla_decode_unabsorbed(q_c, q_r, c_kv, k_r, w_uk, w_uv, seqlens, scale: float
             a = softmax_rows(s[None, :])[0]
             out[b, h] = a @ vh
     return out
+
+
+def mla_prefill_unabsorbed(q_c, q_r, c_kv, k_r, w_uk, w_uv, *, rope_base: float = 0.0,
+                           scale: float | None = None):
+    """Multi-head Latent Attention prefill on the non-absorbed path ("Transformer
+    与 LLM" slide 06: prefill up-projects instead of absorbing, which would cost
+    ~3.4x the attention FLOPs).
+
+    q_c [B, S, n_h, d_c], q_r [B, S, n_h, d_r] (un-rotated), c_kv [B, S, d_l],
+    k_r [B, S, d_r] (un-rotated, shared by all heads), w_uk / w_uv [n_h, d_l, d_c].
+    Per head h: q = [q_c ; q_r], k = [c_kv @ w_uk[h] ; k_r], v = c_kv @ w_uv[h];
+    the d_r dims of q and k are rotated at their positions (decoupled RoPE) when
+    rope_base > 0; scale defaults to 1/sqrt(d_c + d_r).  Returns (q, k, v, out):
+    the per-head tensors [B, S, n_h, d_c + d_r] / [B, S, n_h, d_c] it built, and
+    out [B, S, n_h, d_c] of causal attention over them.
+    """
+    q_c, q_r, c_kv, k_r = _f64(q_c), _f64(q_r), _f64(c_kv), _f64(k_r)
+    w_uk, w_uv = _f64(w_uk), _f64(w_uv)
+    n_h, d_c, d_r = q_c.shape[2], q_c.shape[3], q_r.shape[3]
+    k_c = np.einsum("bsl,hlc->bshc", c_kv, w_uk)            # [B, S, n_h, d_c]
+    v = np.einsum("bsl,hlc->bshc", c_kv, w_uv)
+    k_rh = np.broadcast_to(k_r[:, :, None, :], k_r.shape[:2] + (n_h, d_r))
+    q = np.concatenate([q_c, q_r], axis=-1)
+    k = np.concatenate([k_c, k_rh], axis=-1)
+    scale = 1.0 / math.sqrt(d_c + d_r) if scale is None else scale
+    out = attention_prefill(q, k, v, rope_base=rope_base, scale=scale, rope_offset=d_c, rope_dims=d_r)
+    return q, k, v, out
 
 
 def mla_absorb_query(q_c, q_r, w_uk) -> np.ndarray:

@@ -35,7 +35,7 @@ def declared_symbols():
 def test_header_and_binding_agree():
     names = set(declared_symbols())
     assert names == {n for n, _, _ in B.SIGNATURES}
-    assert len(names) == 14
+    assert len(names) == 15
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -144,3 +144,35 @@ def test_kv_append_argument_errors(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 1e4, 4, 56, 1, None) == -1   # offset not a multiple of 8
     assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 1e4, 32, 64, 1, None) == -1  # span past D_qk
     assert f(MISALIGNED, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 0.0, 0, 64, 1, None) == -3
+
+
+def test_rope_half_flag_validation(lib):
+    HALF = B.ATTN_ROPE_HALF
+    assert HALF == 0x100
+    # unknown flag bits or element types are argument errors
+    assert prefill(lib, dtype=1 | 0x200) == -1
+    assert prefill(lib, dtype=HALF | 2) == -1
+    assert decode(lib, dtype=1 | 0x400) == -1
+    # split halves need whole 8-element chunks per half in bf16 (D_h a multiple of 16)
+    assert prefill(lib, D=8, rope=1e4, dtype=1 | HALF) == -2
+    assert prefill(lib, D=6, rope=1e4, dtype=0 | HALF) == -2   # fp32: D_h a multiple of 4
+    r = lib.attn_rope
+    assert r(FAKE, FAKE, 1, 4, 2, 64, 0, 8, 1e4, 0, 1 | HALF, None) == -1   # a half of 4 bf16 dims
+    assert r(FAKE, FAKE, 1, 4, 2, 64, 0, 6, 1e4, 0, 0 | HALF, None) == -1   # a half of 3 fp32 dims
+    f = lib.attn_kv_append
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 2, 64, 64, 16, 1e4, 0, 8, 1 | HALF, None) == -1
+    # the flag does not change the workspace a decode needs
+    for dt in (0, 1):
+        assert (lib.attn_decode_workspace_size(59, 32, 8, 128, 128, 8192, dt | HALF)
+                == lib.attn_decode_workspace_size(59, 32, 8, 128, 128, 8192, dt))
+
+
+def test_prefill_mla_argument_errors(lib):
+    f = lib.attn_prefill_mla
+    # q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_qk, D_v, rope, roff, rdims, scale, causal, dtype, stream
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE2, None, 1, 16, 2, 2, 192, 128, 1e4, 128, 128, 0.0, 1, 1, None) == -1  # span
+    assert f(FAKE, FAKE, FAKE, FAKE, None, None, 1, 16, 2, 2, 192, 128, 1e4, 128, 64, 0.0, 1, 1, None) == -1   # k_rot
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE2, None, 1, 16, 2, 2, 192, 0, 1e4, 128, 64, 0.0, 1, 1, None) == -1    # D_v
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE2, None, 1, 16, 2, 2, 192, 264, 0.0, 0, 0, 0.0, 1, 1, None) == -2     # D_v > 256
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE2, None, 1, 16, 2, 2, 192, 128, 1e4, 124, 64, 0.0, 1, 1, None) == -2  # offset % 8
+    assert f(FAKE, FAKE, MISALIGNED, FAKE, FAKE2, None, 1, 16, 2, 2, 192, 128, 1e4, 128, 64, 0.0, 1, 1, None) == -3

@@ -284,6 +284,13 @@ def test_prefill_rows_match_full_prefill():
     o, l = oracle.attention_prefill_rows(q, k, v, 1, 3, rows, rope_base=10000.0)
     assert np.allclose(o, full[1, rows, 3], atol=1e-13)
     assert np.allclose(l, lse[1, 3, rows], atol=1e-13)
+    # a RoPE span on part of a 12-dim q/k head and 6-dim values
+    q2 = rng.standard_normal((1, 30, 2, 12))
+    k2 = rng.standard_normal((1, 30, 2, 12))
+    v2 = rng.standard_normal((1, 30, 2, 6))
+    full2 = oracle.attention_prefill(q2, k2, v2, rope_base=100.0, rope_offset=8, rope_dims=4)
+    o2, _ = oracle.attention_prefill_rows(q2, k2, v2, 0, 1, rows[:2], rope_base=100.0, rope_offset=8, rope_dims=4)
+    assert np.allclose(o2, full2[0, rows[:2], 1], atol=1e-13)
 
 
 # ---------------------------------------------------------------- decode
@@ -299,6 +306,37 @@ def test_decode_with_cache_equals_prefill_token_by_token():
     for t in range(S):
         seqlens = np.full(B, t + 1)
         out, _ = oracle.attention_decode(q[:, t], kc, v, seqlens, rope_base=base)
+        assert np.allclose(out, full[:, t], atol=1e-13)
+
+
+def test_half_pairing_attention_is_adjacent_attention_on_permuted_dims():
+    # a score is a dot product, so permuting the dims of q and k alike changes
+    # nothing; the permutation that turns split halves into adjacent pairs
+    # therefore carries half-split attention onto adjacent-pair attention
+    rng = np.random.default_rng(25)
+    B, S, n_h, n_kv, D = 1, 9, 4, 2, 8
+    q = rng.standard_normal((B, S, n_h, D))
+    k = rng.standard_normal((B, S, n_kv, D))
+    v = rng.standard_normal((B, S, n_kv, D))
+    perm = np.array([(j % (D // 2)) * 2 + j // (D // 2) for j in range(D)])
+    qa, ka = np.empty_like(q), np.empty_like(k)
+    qa[..., perm], ka[..., perm] = q, k
+    half = oracle.attention_prefill(q, k, v, rope_base=10000.0, pairing="half")
+    adj = oracle.attention_prefill(qa, ka, v, rope_base=10000.0, pairing="adjacent")
+    assert np.allclose(half, adj, atol=1e-13)
+    assert not np.allclose(half, oracle.attention_prefill(q, k, v, rope_base=10000.0), atol=1e-3)
+
+
+def test_decode_half_pairing_equals_prefill_token_by_token():
+    rng = np.random.default_rng(26)
+    B, S, n_h, n_kv, D = 2, 7, 4, 1, 8
+    q = rng.standard_normal((B, S, n_h, D))
+    k = rng.standard_normal((B, S, n_kv, D))
+    v = rng.standard_normal((B, S, n_kv, D))
+    full = oracle.attention_prefill(q, k, v, rope_base=500.0, pairing="half")
+    kc = oracle.rope_cache(k, 500.0, pairing="half")
+    for t in range(S):
+        out, _ = oracle.attention_decode(q[:, t], kc, v, np.full(B, t + 1), rope_base=500.0, pairing="half")
         assert np.allclose(out, full[:, t], atol=1e-13)
 
 
@@ -323,6 +361,32 @@ def test_mla_absorbed_equals_unabsorbed():
     o_lat, _ = oracle.attention_decode(q_t, cache, cache[..., :512], seqlens, scale=scale)
     out = oracle.mla_unabsorb_output(o_lat, w_uv)
     assert np.max(np.abs(out - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_mla_prefill_unabsorbed_equals_absorbed():
+    # "Transformer 与 LLM" slide 06: the absorbed form (W_UK folded into the query,
+    # W_UV into the output: 128 heads sharing one 576-dim latent KV head) and the
+    # up-projected form the slide routes prefill through give the same attention
+    rng = np.random.default_rng(27)
+    B, S, n_h, d_c, d_r, d_l = 1, 10, 3, 8, 4, 12
+    q_c = rng.standard_normal((B, S, n_h, d_c))
+    q_r = rng.standard_normal((B, S, n_h, d_r))
+    c_kv = rng.standard_normal((B, S, d_l))
+    k_r = rng.standard_normal((B, S, d_r))
+    w_uk = rng.standard_normal((n_h, d_l, d_c)) / math.sqrt(d_l)
+    w_uv = rng.standard_normal((n_h, d_l, d_c)) / math.sqrt(d_l)
+    q, k, v, out = oracle.mla_prefill_unabsorbed(q_c, q_r, c_kv, k_r, w_uk, w_uv, rope_base=100.0)
+    assert q.shape == (B, S, n_h, d_c + d_r) and v.shape == (B, S, n_h, d_c)
+    assert np.array_equal(k[:, :, 0, d_c:], k[:, :, 2, d_c:])   # k^R shared by every head
+    q_abs = np.concatenate([np.einsum("hlc,bshc->bshl", w_uk, q_c), q_r], axis=-1)
+    latent = np.concatenate([c_kv, k_r], axis=-1)[:, :, None, :]  # one KV head of d_l + d_r dims
+    o_lat = oracle.attention_prefill(q_abs, latent, c_kv[:, :, None, :], rope_base=100.0,
+                                     scale=1 / math.sqrt(d_c + d_r), rope_offset=d_l, rope_dims=d_r)
+    absorbed = np.einsum("hlc,bshl->bshc", w_uv, o_lat)
+    assert np.max(np.abs(out - absorbed)) <= 1e-12 * max(1.0, np.max(np.abs(out)))
+    # the RoPE span matters: without rotation the result differs
+    _, _, _, plain = oracle.mla_prefill_unabsorbed(q_c, q_r, c_kv, k_r, w_uk, w_uv)
+    assert np.max(np.abs(out - plain)) > 1e-3
 
 
 def test_hand_example_rows_sum_to_one():

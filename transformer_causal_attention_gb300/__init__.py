@@ -7,6 +7,7 @@ kernels.  Build the library first with ``transformer_causal_attention_gb300.buil
 from ._binding import (  # noqa: F401
     ATTN_BF16,
     ATTN_F32,
+    ATTN_ROPE_HALF,
     AttnError,
     LIB_PATH,
     check_wait_timeout,
@@ -15,6 +16,7 @@ from ._binding import (  # noqa: F401
     decode_workspace_size,
     kv_append,
     prefill_chunk,
+    prefill_mla,
     prefill_window,
     device_status,
     launch_count,

@@ -17,6 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_F32, ATTN_BF16 = 0, 1
+ATTN_ROPE_HALF = 0x100  # OR'd into the dtype code: RoPE pairs (j, j + rope_dims/2)
 ERRORS = {
     0: "ATTN_OK", -1: "ATTN_ERR_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_ALIGN",
     -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_TIMEOUT", -6: "ATTN_ERR_WORKSPACE",
@@ -28,6 +29,8 @@ SIGNATURES = [
     ("attn_strerror", ctypes.c_char_p, [_i]),
     ("attn_prefill", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
     ("attn_prefill_window", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i, _i, _i, _vp]),
+    ("attn_prefill_mla", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i, _i,
+                              _vp]),
     ("attn_rope", _i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     ("attn_prefill_chunk", _i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
     ("attn_kv_append", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
@@ -82,11 +85,15 @@ def _check(rc: int, where: str) -> None:
         raise AttnError(rc, where)
 
 
-def _dtype_code(t: torch.Tensor) -> int:
+def _dtype_code(t: torch.Tensor, pairing: str = "adjacent") -> int:
+    """Element-type code of t, with ATTN_ROPE_HALF for pairing="half"."""
+    if pairing not in ("adjacent", "half"):
+        raise ValueError(f"pairing must be 'adjacent' or 'half', not {pairing!r}")
+    flag = ATTN_ROPE_HALF if pairing == "half" else 0
     if t.dtype == torch.bfloat16:
-        return ATTN_BF16
+        return ATTN_BF16 | flag
     if t.dtype == torch.float32:
-        return ATTN_F32
+        return ATTN_F32 | flag
     raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
 
 
@@ -108,13 +115,14 @@ def _ptr(t: torch.Tensor | None):
 
 
 def prefill(q, k, v, *, rope_base: float = 0.0, scale: float = 0.0, causal: bool = True,
-            out=None, k_rot=None, lse: bool | torch.Tensor = False, stream=None):
+            out=None, k_rot=None, lse: bool | torch.Tensor = False, pairing: str = "adjacent", stream=None):
     """Causal (or full) attention over whole prompts via attn_prefill.
 
     q [B,S,n_h,D], k/v [B,S,n_kv,D] CUDA tensors (bf16 or fp32, contiguous, BSHD).
     Returns out [B,S,n_h,D]; with rope_base > 0 also returns the rotated keys
     k_rot [B,S,n_kv,D] (the KV-cache form), and with lse=True the fp32
     log-sum-exp [B,n_h,S].  Result tuple: (out, k_rot or None, lse or None).
+    pairing "adjacent" rotates dims (2i, 2i+1), "half" dims (j, j + D/2).
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
         _dev(t, name)
@@ -137,13 +145,13 @@ def prefill(q, k, v, *, rope_base: float = 0.0, scale: float = 0.0, causal: bool
         lse_t = None
     rc = _lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(k_rot) if rope_base > 0 else None,
                              _ptr(lse_t), B, S, n_h, n_kv, D, float(rope_base), float(scale),
-                             1 if causal else 0, _dtype_code(q), _stream_ptr(stream))
+                             1 if causal else 0, _dtype_code(q, pairing), _stream_ptr(stream))
     _check(rc, "attn_prefill")
     return out, (k_rot if rope_base > 0 else None), lse_t
 
 
 def prefill_window(q, k, v, *, window: int, n_sink: int = 0, rope_base: float = 0.0, scale: float = 0.0,
-                   out=None, k_rot=None, lse: bool = False, stream=None):
+                   out=None, k_rot=None, lse: bool = False, pairing: str = "adjacent", stream=None):
     """Causal sliding-window attention with attention sinks via attn_prefill_window.
 
     Same tensors as prefill(); a query at position m sees keys n <= m with
@@ -160,13 +168,47 @@ def prefill_window(q, k, v, *, window: int, n_sink: int = 0, rope_base: float = 
     lse_t = torch.empty((B, n_h, S), dtype=torch.float32, device=q.device) if lse else None
     rc = _lib().attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(k_rot) if rope_base > 0 else None,
                                     _ptr(lse_t), B, S, n_h, n_kv, D, float(rope_base), float(scale), int(window),
-                                    int(n_sink), _dtype_code(q), _stream_ptr(stream))
+                                    int(n_sink), _dtype_code(q, pairing), _stream_ptr(stream))
     _check(rc, "attn_prefill_window")
     return out, (k_rot if rope_base > 0 else None), lse_t
 
 
+def prefill_mla(q, k, v, *, rope_base: float = 0.0, rope_offset: int = 0, rope_dims: int | None = None,
+                scale: float = 0.0, causal: bool = True, out=None, k_rot=None, lse: bool | torch.Tensor = False,
+                pairing: str = "adjacent", stream=None):
+    """Prefill with q/k head dim D_qk != v head dim D_v and RoPE on a span (attn_prefill_mla).
+
+    q [B,S,n_h,D_qk], k [B,S,n_kv,D_qk], v [B,S,n_kv,D_v].  For the MLA prefill
+    shape D_qk = 192 (content 128 + decoupled RoPE 64, rope_offset=128,
+    rope_dims=64) and D_v = 128.  Returns (out [B,S,n_h,D_v], k_rot or None, lse or None).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share a dtype")
+    B, S, n_h, D_qk = q.shape
+    n_kv, D_v = k.shape[2], v.shape[3]
+    if k.shape != (B, S, n_kv, D_qk) or v.shape != (B, S, n_kv, D_v):
+        raise ValueError("k must be [B, S, n_kv, D_qk] and v [B, S, n_kv, D_v]")
+    rope_dims = (D_qk - rope_offset) if rope_dims is None else rope_dims
+    if out is None:
+        out = torch.empty((B, S, n_h, D_v), dtype=q.dtype, device=q.device)
+    _dev(out, "out")
+    if rope_base > 0 and k_rot is None:
+        k_rot = torch.empty_like(k)
+    if isinstance(lse, torch.Tensor):
+        lse_t = lse
+    else:
+        lse_t = torch.empty((B, n_h, S), dtype=torch.float32, device=q.device) if lse else None
+    rc = _lib().attn_prefill_mla(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(k_rot) if rope_base > 0 else None,
+                                 _ptr(lse_t), B, S, n_h, n_kv, D_qk, D_v, float(rope_base), rope_offset, rope_dims,
+                                 float(scale), 1 if causal else 0, _dtype_code(q, pairing), _stream_ptr(stream))
+    _check(rc, "attn_prefill_mla")
+    return out, (k_rot if rope_base > 0 else None), lse_t
+
+
 def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = None, pos_offset: int = 0,
-         out=None, stream=None):
+         out=None, pairing: str = "adjacent", stream=None):
     """RoPE of x [B,S,n_heads,D] at positions pos_offset + s via attn_rope (out may be x)."""
     _dev(x, "x")
     B, S, H, D = x.shape
@@ -174,13 +216,13 @@ def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = N
     if out is None:
         out = torch.empty_like(x)
     rc = _lib().attn_rope(_ptr(out), _ptr(x), B, S, H, D, rope_offset, rope_dims, float(rope_base), pos_offset,
-                          _dtype_code(x), _stream_ptr(stream))
+                          _dtype_code(x, pairing), _stream_ptr(stream))
     _check(rc, "attn_rope")
     return out
 
 
 def prefill_chunk(q, kcache, vcache, *, q_offset: int, rope_base: float = 0.0, scale: float = 0.0,
-                  causal: bool = True, out=None, lse: bool = False, stream=None):
+                  causal: bool = True, out=None, lse: bool = False, pairing: str = "adjacent", stream=None):
     """A prompt chunk at positions q_offset.. against a KV cache via attn_prefill_chunk.
 
     q [B,S_q,n_h,D] (un-rotated), kcache/vcache [B,max_len,n_kv,D] holding rotated keys
@@ -197,13 +239,13 @@ def prefill_chunk(q, kcache, vcache, *, q_offset: int, rope_base: float = 0.0, s
     lse_t = torch.empty((B, n_h, S_q), dtype=torch.float32, device=q.device) if lse else None
     rc = _lib().attn_prefill_chunk(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), _ptr(lse_t), B, S_q, q_offset,
                                    max_len, n_h, n_kv, D, float(rope_base), float(scale), 1 if causal else 0,
-                                   _dtype_code(q), _stream_ptr(stream))
+                                   _dtype_code(q, pairing), _stream_ptr(stream))
     _check(rc, "attn_prefill_chunk")
     return out, lse_t
 
 
 def kv_append(k_new, v_new, kcache, vcache, start, *, rope_base: float = 0.0, rope_offset: int = 0,
-              rope_dims: int | None = None, stream=None):
+              rope_dims: int | None = None, pairing: str = "adjacent", stream=None):
     """Write new tokens into a KV cache via attn_kv_append (keys rotated at start[b] + c).
 
     k_new [B,C,n_kv,D_qk], v_new [B,C,n_kv,D_v] or None (values alias the keys),
@@ -226,7 +268,7 @@ def kv_append(k_new, v_new, kcache, vcache, start, *, rope_base: float = 0.0, ro
     rope_dims = (D_qk - rope_offset) if rope_dims is None else rope_dims
     rc = _lib().attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kcache), None if vcache is None else vcache.data_ptr(),
                                ldv, _ptr(start), B, C, n_kv, D_qk, D_v, max_len, float(rope_base), rope_offset,
-                               rope_dims, _dtype_code(k_new), _stream_ptr(stream))
+                               rope_dims, _dtype_code(k_new, pairing), _stream_ptr(stream))
     _check(rc, "attn_kv_append")
 
 
@@ -240,7 +282,7 @@ def decode_workspace_size(B, n_h, n_kv, D_qk, D_v, max_len, dtype=torch.bfloat16
 
 def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: int = 0,
            rope_dims: int | None = None, scale: float = 0.0, out=None, lse: bool = False, workspace=None,
-           stream=None, _window=None):
+           pairing: str = "adjacent", stream=None, _window=None):
     """One new token per sequence against its KV cache via attn_decode.
 
     q [B,n_h,D_qk] (un-rotated), kcache [B,L,n_kv,D_qk] (rotated keys), vcache
@@ -272,7 +314,7 @@ def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: i
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     common = (_ptr(q), _ptr(kcache), vcache.data_ptr(), ldv, _ptr(seqlens), _ptr(out), _ptr(lse_t), B, n_h, n_kv,
               D_qk, D_v, L, float(rope_base), rope_offset, rope_dims, float(scale))
-    tail = (_dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    tail = (_dtype_code(q, pairing), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if _window is None:
         _check(_lib().attn_decode(*common, *tail), "attn_decode")
     else:
@@ -282,10 +324,11 @@ def decode(q, kcache, vcache, seqlens, *, rope_base: float = 0.0, rope_offset: i
 
 def decode_window(q, kcache, vcache, seqlens, *, window: int, n_sink: int = 0, rope_base: float = 0.0,
                   rope_offset: int = 0, rope_dims: int | None = None, scale: float = 0.0, out=None,
-                  lse: bool = False, workspace=None, stream=None):
+                  lse: bool = False, workspace=None, pairing: str = "adjacent", stream=None):
     """decode() with a sliding window of `window` keys plus `n_sink` sink keys (attn_decode_window)."""
     return decode(q, kcache, vcache, seqlens, rope_base=rope_base, rope_offset=rope_offset, rope_dims=rope_dims,
-                  scale=scale, out=out, lse=lse, workspace=workspace, stream=stream, _window=(window, n_sink))
+                  scale=scale, out=out, lse=lse, workspace=workspace, pairing=pairing, stream=stream,
+                  _window=(window, n_sink))
 
 
 def device_status(stream=None) -> int:

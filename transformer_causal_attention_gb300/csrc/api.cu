@@ -96,8 +96,8 @@ bool make_map3(CUtensorMap* map, const void* base, int D, int rows, int B, unsig
 }
 
 // MLA shape served by the tensor-core decode kernel (one 576-dim latent head, V = its first 512 dims).
-bool mla_shape(int B, int n_h, int n_kv, int D_qk, int D_v, attn_dtype_t dtype) {
-  return dtype == ATTN_BF16 && n_h == 128 && n_kv == 1 && D_qk == 576 && D_v == 512 && B <= 1024;
+bool mla_shape(int B, int n_h, int n_kv, int D_qk, int D_v, bool bf16) {
+  return bf16 && n_h == 128 && n_kv == 1 && D_qk == 576 && D_v == 512 && B <= 1024;
 }
 
 // Dense BSHD tensor [B, S, heads, D], boxes of 128 positions.
@@ -106,12 +106,25 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int heads, 
   return make_map4(map, base, D, heads, S, B, hs, hs * heads, hs * heads * S, 128);
 }
 
+// The dtype argument: element type in the low byte, ATTN_ROPE_HALF optionally
+// OR'd in.  False for anything else.
+bool parse_dtype(attn_dtype_t dtype, bool* bf16, bool* half) {
+  const unsigned d = static_cast<unsigned>(dtype);
+  const unsigned elem = d & 0xffu, flags = d & ~0xffu;
+  if (elem != ATTN_F32 && elem != ATTN_BF16) return false;
+  if (flags & ~static_cast<unsigned>(ATTN_ROPE_HALF)) return false;
+  *bf16 = elem == ATTN_BF16;
+  *half = flags != 0;
+  return true;
+}
+
 // theta_i = base^(-2i/dims) expressed in turns per position, split hi + lo.
-RopeFreq make_rope(float base, int dims) {
+RopeFreq make_rope(float base, int dims, bool half) {
   RopeFreq f;
   memset(&f, 0, sizeof(f));
   if (!(base > 0.f) || dims <= 0) return f;
   f.n_pairs = dims / 2;
+  f.half = half ? 1 : 0;
   const double two_pi = 6.283185307179586476925286766559;
   for (int i = 0; i < f.n_pairs; ++i) {
     const double turns = pow(static_cast<double>(base), -2.0 * i / dims) / two_pi;
@@ -173,42 +186,51 @@ const char* attn_strerror(int code) {
 int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D, int rope_offset, int rope_dims,
               float rope_base, int pos_offset, attn_dtype_t dtype, void* stream) {
   if (!x_out || !x_in || B <= 0 || S <= 0 || n_heads <= 0 || D <= 0) return ATTN_ERR_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
   if (!(rope_base > 0.f) || rope_offset < 0 || rope_dims <= 0 || rope_offset + rope_dims > D || pos_offset < 0)
     return ATTN_ERR_ARG;
-  const int unit = dtype == ATTN_BF16 ? 8 : 2;
-  if (D % unit || rope_offset % unit || rope_dims % unit) return ATTN_ERR_ARG;
+  const int unit = bf16 ? 8 : 2;  // a thread's chunk of dims; with half pairing each half is whole chunks
+  if (D % unit || rope_offset % unit || rope_dims % (half ? 2 * unit : unit)) return ATTN_ERR_ARG;
   if (rope_dims / 2 > kMaxRopePairs) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(x_out) || !aligned16(x_in)) return ATTN_ERR_ALIGN;
-  const size_t bytes = static_cast<size_t>(B) * S * n_heads * D * (dtype == ATTN_BF16 ? 2 : 4);
+  const size_t bytes = static_cast<size_t>(B) * S * n_heads * D * (bf16 ? 2 : 4);
   if (x_out != x_in && overlap(x_out, bytes, x_in, bytes)) return ATTN_ERR_ARG;
   RopeArgs ra{x_out, x_in, B, S, n_heads, D, rope_offset, rope_dims, pos_offset};
   int launches = 0;
   const cudaError_t e =
-      launch_rope(ra, make_rope(rope_base, rope_dims), dtype == ATTN_BF16, static_cast<cudaStream_t>(stream), &launches);
+      launch_rope(ra, make_rope(rope_base, rope_dims, half), bf16, static_cast<cudaStream_t>(stream), &launches);
   return finish(e, launches);
 }
 
 namespace attn {
 namespace {
 int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
-                 int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, int window, int n_sink,
-                 attn_dtype_t dtype, void* stream);
+                 int n_h, int n_kv, int D_qk, int D_v, float rope_base, int rope_offset, int rope_dims, float scale,
+                 int causal, int window, int n_sink, attn_dtype_t dtype, void* stream);
 }  // namespace
 }  // namespace attn
 
 int attn_prefill(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
                  int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, attn_dtype_t dtype,
                  void* stream) {
-  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, rope_base, scale, causal, 0, 0, dtype, stream);
+  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, D_h, rope_base, 0, D_h, scale, causal, 0, 0,
+                      dtype, stream);
 }
 
 int attn_prefill_window(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B,
                         int S, int n_h, int n_kv, int D_h, float rope_base, float scale, int window, int n_sink,
                         attn_dtype_t dtype, void* stream) {
   if (window <= 0 || n_sink < 0) return ATTN_ERR_ARG;
-  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, rope_base, scale, 1, window, n_sink, dtype,
-                      stream);
+  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_h, D_h, rope_base, 0, D_h, scale, 1, window,
+                      n_sink, dtype, stream);
+}
+
+int attn_prefill_mla(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
+                     int n_h, int n_kv, int D_qk, int D_v, float rope_base, int rope_offset, int rope_dims,
+                     float scale, int causal, attn_dtype_t dtype, void* stream) {
+  return prefill_impl(q, k, v, out, k_rot, lse, B, S, n_h, n_kv, D_qk, D_v, rope_base, rope_offset, rope_dims, scale,
+                      causal, 0, 0, dtype, stream);
 }
 
 }  // extern "C"
@@ -216,41 +238,46 @@ int attn_prefill_window(const void* q, const void* k, const void* v, void* out, 
 namespace attn {
 namespace {
 int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k_rot, float* lse, int B, int S,
-                 int n_h, int n_kv, int D_h, float rope_base, float scale, int causal, int window, int n_sink,
-                 attn_dtype_t dtype, void* stream) {
+                 int n_h, int n_kv, int D_qk, int D_v, float rope_base, int rope_offset, int rope_dims, float scale,
+                 int causal, int window, int n_sink, attn_dtype_t dtype, void* stream) {
   if (!q || !k || !v || !out) return ATTN_ERR_ARG;
-  if (B <= 0 || S <= 0 || n_h <= 0 || n_kv <= 0 || D_h <= 0 || n_h % n_kv) return ATTN_ERR_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  if (B <= 0 || S <= 0 || n_h <= 0 || n_kv <= 0 || D_qk <= 0 || D_v <= 0 || n_h % n_kv) return ATTN_ERR_ARG;
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
-  const bool bf16 = dtype == ATTN_BF16;
-  if (D_h > 256 || D_h % (bf16 ? 8 : 2)) return ATTN_ERR_UNSUPPORTED;
   const bool rope = rope_base > 0.f;
+  const int unit = bf16 ? 8 : 2;  // vector width of the kernels' loads, in elements
+  if (rope && (rope_offset < 0 || rope_dims <= 0 || rope_offset + rope_dims > D_qk)) return ATTN_ERR_ARG;
+  if (D_qk > 256 || D_v > 256 || D_qk % unit || D_v % unit) return ATTN_ERR_UNSUPPORTED;
+  if (rope && (rope_offset % unit || rope_dims % (half ? 2 * unit : unit))) return ATTN_ERR_UNSUPPORTED;
+  if (rope && rope_dims / 2 > kMaxRopePairs) return ATTN_ERR_UNSUPPORTED;
   if (rope && !k_rot) return ATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (rope && !aligned16(k_rot)) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_ALIGN;
   const size_t esz = bf16 ? 2 : 4;
-  const size_t kv_bytes = static_cast<size_t>(B) * S * n_kv * D_h * esz;
-  if (rope && overlap(k_rot, kv_bytes, k, kv_bytes)) return ATTN_ERR_ARG;
+  const size_t k_bytes = static_cast<size_t>(B) * S * n_kv * D_qk * esz;
+  if (rope && overlap(k_rot, k_bytes, k, k_bytes)) return ATTN_ERR_ARG;
 
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_h));
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_qk));
   int launches = 0;
   cudaError_t e = cudaSuccess;
-  const RopeFreq rf = make_rope(rope_base, D_h);
+  const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0, half);
   if (rope) {
-    RopeArgs ra{k_rot, k, B, S, n_kv, D_h, 0, D_h, 0};
+    // rotated keys, written once: the form a KV cache stores
+    RopeArgs ra{k_rot, k, B, S, n_kv, D_qk, rope_offset, rope_dims, 0};
     e = launch_rope(ra, rf, bf16, st, &launches);
     if (e != cudaSuccess) return finish(e, launches);
   }
-  PrefillArgs pa{q, rope ? k_rot : k, v, out, lse, B, S, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
-                 g_wait_limit_ns.load(), S, 0, S, window, n_sink};
-  if (prefill_tc_supported(D_h, bf16)) {
+  PrefillArgs pa{q, rope ? k_rot : k, v, out, lse, B, S, n_h, n_kv, D_qk, sc * kLog2e, causal, dev.status,
+                 g_wait_limit_ns.load(), S, 0, S, window, n_sink, D_v, rope ? rope_offset : 0};
+  if (prefill_tc_supported(D_qk, D_v, bf16)) {
     CUtensorMap maps[3];
-    if (!make_bshd_map(&maps[0], q, B, S, n_h, D_h) || !make_bshd_map(&maps[1], pa.k, B, S, n_kv, D_h) ||
-        !make_bshd_map(&maps[2], v, B, S, n_kv, D_h))
+    if (!make_bshd_map(&maps[0], q, B, S, n_h, D_qk) || !make_bshd_map(&maps[1], pa.k, B, S, n_kv, D_qk) ||
+        !make_bshd_map(&maps[2], v, B, S, n_kv, D_v))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_prefill_tc(pa, rf, maps, dev.sms, st, &launches);
   } else {
@@ -270,10 +297,10 @@ int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, vo
   if (!q || !kcache || !vcache || !out) return ATTN_ERR_ARG;
   if (B <= 0 || S_q <= 0 || n_h <= 0 || n_kv <= 0 || D_h <= 0 || n_h % n_kv) return ATTN_ERR_ARG;
   if (q_offset < 0 || max_len <= 0 || static_cast<long long>(q_offset) + S_q > max_len) return ATTN_ERR_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
-  const bool bf16 = dtype == ATTN_BF16;
-  if (D_h > 256 || D_h % (bf16 ? 8 : 2)) return ATTN_ERR_UNSUPPORTED;
+  if (D_h > 256 || D_h % ((bf16 ? 8 : 2) * (rope_base > 0.f && half ? 2 : 1))) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_ALIGN;
@@ -283,11 +310,11 @@ int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, vo
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_h));
   const int S_k = q_offset + S_q;
   PrefillArgs pa{q, kcache, vcache, out, lse, B, S_q, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
-                 g_wait_limit_ns.load(), S_k, q_offset, max_len};
-  const RopeFreq rf = make_rope(rope_base, D_h);
+                 g_wait_limit_ns.load(), S_k, q_offset, max_len, 0, 0, D_h, 0};
+  const RopeFreq rf = make_rope(rope_base, D_h, half);
   int launches = 0;
   cudaError_t e;
-  if (prefill_tc_supported(D_h, bf16)) {
+  if (prefill_tc_supported(D_h, D_h, bf16)) {
     // K/V maps cover only the S_k visible rows of each sequence: rows past them read as zero
     CUtensorMap maps[3];
     const unsigned long long hs = static_cast<unsigned long long>(D_h) * 2;
@@ -308,10 +335,12 @@ int attn_kv_append(const void* k_new, const void* v_new, void* kcache, void* vca
   if (!k_new || !kcache || !start || (v_new && !vcache)) return ATTN_ERR_ARG;
   if (B <= 0 || C <= 0 || n_kv <= 0 || D_qk <= 0 || D_v <= 0 || max_len <= 0 || v_token_stride < 0)
     return ATTN_ERR_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
   if (D_qk % 8 || D_v % 8) return ATTN_ERR_ARG;
   const bool rope = rope_base > 0.f;
-  if (rope && (rope_offset < 0 || rope_dims <= 0 || rope_offset % 8 || rope_dims % 8 || rope_offset + rope_dims > D_qk))
+  if (rope && (rope_offset < 0 || rope_dims <= 0 || rope_offset % 8 || rope_dims % (half ? 16 : 8) ||
+               rope_offset + rope_dims > D_qk))
     return ATTN_ERR_ARG;
   if (rope && rope_dims / 2 > kMaxRopePairs) return ATTN_ERR_UNSUPPORTED;
   const long long ldv = v_token_stride ? v_token_stride : static_cast<long long>(n_kv) * D_v;
@@ -320,18 +349,19 @@ int attn_kv_append(const void* k_new, const void* v_new, void* kcache, void* vca
     return ATTN_ERR_ALIGN;
   KvAppendArgs ka{k_new, v_new, kcache, vcache, ldv, start, B, C, n_kv, D_qk, D_v, max_len, rope ? rope_offset : 0};
   int launches = 0;
-  const cudaError_t e = launch_kv_append(ka, make_rope(rope_base, rope ? rope_dims : 0), dtype == ATTN_BF16,
+  const cudaError_t e = launch_kv_append(ka, make_rope(rope_base, rope ? rope_dims : 0, half), bf16,
                                          static_cast<cudaStream_t>(stream), &launches);
   return finish(e, launches);
 }
 
 size_t attn_decode_workspace_size(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len, attn_dtype_t dtype) {
   if (B <= 0 || n_h <= 0 || n_kv <= 0 || n_h % n_kv || D_qk <= 0 || D_v <= 0 || max_len <= 0) return static_cast<size_t>(-1);
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return static_cast<size_t>(-1);
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return static_cast<size_t>(-1);
   int chunk = 0;
   const int ns = decode_plan_splits(B, n_h, n_kv, D_qk, D_v, max_len, &chunk);
   size_t slots = static_cast<size_t>(B) * n_h * ns;
-  if (mla_shape(B, n_h, n_kv, D_qk, D_v, dtype)) {
+  if (mla_shape(B, n_h, n_kv, D_qk, D_v, bf16)) {
     // one partial per (pair, sequence) piece: at most pairs + B - 1 of them
     const size_t mla_slots = static_cast<size_t>(kMlaMaxPairs + B) * n_h;
     if (mla_slots > slots) slots = mla_slots;
@@ -377,7 +407,8 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !kcache || !vcache || !seqlens || !out || !workspace) return ATTN_ERR_ARG;
   if (B <= 0 || n_h <= 0 || n_kv <= 0 || n_h % n_kv || D_qk <= 0 || D_v <= 0 || max_len <= 0) return ATTN_ERR_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_ARG;
+  bool bf16 = false, half = false;
+  if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
   if (v_token_stride < 0) return ATTN_ERR_ARG;
   const long long ldv = v_token_stride ? v_token_stride : static_cast<long long>(n_kv) * D_v;
   if (ldv < static_cast<long long>(n_kv) * D_v && vcache != kcache) return ATTN_ERR_ARG;
@@ -399,16 +430,18 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   int chunk = 0;
   int ns = decode_plan_splits(B, n_h, n_kv, D_qk, D_v, max_len, &chunk);
   size_t slots = static_cast<size_t>(B) * n_h * ns;
-  if (mla_shape(B, n_h, n_kv, D_qk, D_v, dtype)) {
+  if (mla_shape(B, n_h, n_kv, D_qk, D_v, bf16)) {
     const size_t mla_slots = static_cast<size_t>(kMlaMaxPairs + B) * n_h;
     if (mla_slots > slots) slots = mla_slots;
   }
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            ((slots * D_v * sizeof(float) + 255) & ~size_t(255)));
-  const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, dtype) &&
-                       decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, dtype == ATTN_BF16) &&
-                       (!rope || (rope_offset % 8 == 0 && rope_dims % 8 == 0 && rope_offset >= 384));
+  // the tensor-core and streaming kernels rotate whole 8-dim chunks of the query
+  const bool chunked_rope = !rope || (rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0);
+  const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, bf16) &&
+                       decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, bf16) &&
+                       chunked_rope && (!rope || rope_offset >= 384);
   if (use_mla) {
     ns = decode_mla_pairs(dev.sms);  // the kernel runs 2 CTAs per pair
     chunk = 0;
@@ -418,8 +451,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
                 rope ? rope_offset : 0, sc * kLog2e, ws_o, ws_lse, ns, chunk, dev.status, g_wait_limit_ns.load(),
                 window, n_sink};
   int launches = 0;
-  const bool bf16 = dtype == ATTN_BF16;
-  const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0);
+  const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0, half);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (use_mla) {
@@ -429,7 +461,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
         !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, 32))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);
-  } else if (window == 0 && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
+  } else if (window == 0 && chunked_rope && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
     // K and V stream through shared memory in 64-key tiles
     CUtensorMap maps[2];
     const unsigned long long ks = static_cast<unsigned long long>(D_qk) * 2;

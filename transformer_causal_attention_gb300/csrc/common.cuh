@@ -18,12 +18,21 @@ enum : unsigned int { STATUS_TIMEOUT = 1u };
 // Frequencies of the RoPE pairs, in turns per position: f_i = theta_i / (2*pi)
 // with theta_i = base^(-2i / D_r).  Each f_i is split into hi + lo floats by the
 // host (computed in double) so that pos * f_i keeps ~48 bits before reduction.
+// Pair p of a rotated span of 2 * n_pairs dims is (2p, 2p + 1) within the span,
+// or with `half` set (p, p + n_pairs): the split-halves layout.  Either way it
+// turns by pos * theta_p.
 constexpr int kMaxRopePairs = 128;
 struct RopeFreq {
   int n_pairs;  // 0: no rotation
+  int half;     // 1: pair p is (p, p + n_pairs); 0: (2p, 2p + 1)
   float hi[kMaxRopePairs];
   float lo[kMaxRopePairs];
 };
+
+// Span-relative dims of rotation pair p.
+__device__ __forceinline__ int2 rope_pair_dims(const RopeFreq& f, int p) {
+  return f.half ? make_int2(p, p + f.n_pairs) : make_int2(2 * p, 2 * p + 1);
+}
 
 // sin/cos of the angle pos * theta_i.  The product pos * f_i (turns) is formed
 // with an exact two-product, its integer part removed exactly (Sterbenz), and
@@ -52,6 +61,13 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // 8 bf16 packed in a uint4 <-> 8 floats.  bf16 is the upper half of an fp32,
@@ -238,6 +254,14 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Per-warpgroup register budget (all warps of a warpgroup execute the same one).
+template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N> __device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {

@@ -76,21 +76,29 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a, Ro
   // rotated, pre-scaled queries of the HG heads
   const T* qb = static_cast<const T*>(a.q) + (static_cast<long long>(b) * a.n_h + h0) * a.D_qk;
   for (int idx = threadIdx.x; idx < HG * (NQC * 64); idx += kThreads) {
+    // pair slot p covers dims (2p, 2p + 1), except inside the rotated span
+    // (rope_offset is even) where it is rotation pair j = p - rope_offset / 2
     const int i = idx / (NQC * 64), p = idx % (NQC * 64);
-    const int d = 2 * p;
+    const int j = p - a.rope_offset / 2;
+    const bool rot = j >= 0 && j < f.n_pairs;
+    int2 d = make_int2(2 * p, 2 * p + 1);
+    if (rot) {
+      d = rope_pair_dims(f, j);
+      d.x += a.rope_offset;
+      d.y += a.rope_offset;
+    }
     float x0 = 0.f, x1 = 0.f;
-    if (d < a.D_qk) {
-      x0 = to_f32(qb[i * a.D_qk + d]);
-      x1 = to_f32(qb[i * a.D_qk + d + 1]);
-      const int rp = (d - a.rope_offset) / 2;
-      if (d >= a.rope_offset && rp < f.n_pairs) {
+    if (2 * p < a.D_qk) {
+      x0 = to_f32(qb[i * a.D_qk + d.x]);
+      x1 = to_f32(qb[i * a.D_qk + d.y]);
+      if (rot) {
         float s, c;
-        rope_sincos(pos, f.hi[rp], f.lo[rp], &s, &c);
+        rope_sincos(pos, f.hi[j], f.lo[j], &s, &c);
         rotate_pair(x0, x1, s, c);
       }
     }
-    q_s[i * NQC * 128 + d] = x0 * a.scale_log2;
-    q_s[i * NQC * 128 + d + 1] = x1 * a.scale_log2;
+    q_s[i * NQC * 128 + d.x] = x0 * a.scale_log2;
+    q_s[i * NQC * 128 + d.y] = x1 * a.scale_log2;
   }
   __syncthreads();
 

@@ -364,18 +364,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rotate this head's dims [rope_offset, rope_offset + rope_dims) (all in the shared-memory
         // part) at the new token's position
         uint8_t* row = smem + kQOff + h * 128;
-        for (int c = (a.rope_offset - kQTmemDims) / 8; c < (a.rope_offset + 2 * f.n_pairs - kQTmemDims) / 8; ++c) {
-          uint4* ptr = reinterpret_cast<uint4*>(row + (c >> 3) * kQBlockBytes + (((c & 7) ^ (h & 7)) << 4));
-          float x[8];
-          bf16x8_to_f32(*ptr, x);
+        auto chunk = [&](int c) {
+          return reinterpret_cast<uint4*>(row + (c >> 3) * kQBlockBytes + (((c & 7) ^ (h & 7)) << 4));
+        };
+        const int c0 = (a.rope_offset - kQTmemDims) / 8;  // first chunk of the span
+        if (f.half) {
+          // pair j = span dims (j, j + n_pairs): chunk c0 + i holds first members, chunk c0 + i + n_pairs / 8
+          // the second ones (n_pairs % 8 == 0)
+          for (int i = 0; i < f.n_pairs / 8; ++i) {
+            uint4* p0 = chunk(c0 + i);
+            uint4* p1 = chunk(c0 + i + f.n_pairs / 8);
+            float x0[8], x1[8];
+            bf16x8_to_f32(*p0, x0);
+            bf16x8_to_f32(*p1, x1);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rp = (kQTmemDims + c * 8 + 2 * e - a.rope_offset) / 2;
-            float sn, cs;
-            rope_sincos(L - 1, f.hi[rp], f.lo[rp], &sn, &cs);
-            rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
+            for (int e = 0; e < 8; ++e) {
+              float sn, cs;
+              rope_sincos(L - 1, f.hi[i * 8 + e], f.lo[i * 8 + e], &sn, &cs);
+              rotate_pair(x0[e], x1[e], sn, cs);
+            }
+            *p0 = f32_to_bf16x8(x0);
+            *p1 = f32_to_bf16x8(x1);
           }
-          *ptr = f32_to_bf16x8(x);
+        } else {
+          for (int i = 0; i < f.n_pairs / 4; ++i) {
+            uint4* ptr = chunk(c0 + i);
+            float x[8];
+            bf16x8_to_f32(*ptr, x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float sn, cs;
+              rope_sincos(L - 1, f.hi[i * 4 + e], f.lo[i * 4 + e], &sn, &cs);
+              rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
+            }
+            *ptr = f32_to_bf16x8(x);
+          }
         }
         fence_proxy_async_smem();
       }

@@ -167,27 +167,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = w.L - 1;  // the new token's position
       // this lane's 8 query dims of each head, rotated at the new token's position and pre-scaled
       float2 q2[HG][4];
-      {
+      const __nv_bfloat16* qb =
+          static_cast<const __nv_bfloat16*>(a.q) + (static_cast<long long>(w.b) * a.n_h + w.h0) * D + hl * 8;
+      const int rel = hl * 8 - a.rope_offset;  // this lane's chunk within the rotated span (offset % 8 == 0)
+      const bool in_span = rel >= 0 && rel < 2 * f.n_pairs;
+      if (!f.half) {
         float sn[4], cs[4];
-        bool rot[4];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int d = hl * 8 + 2 * p;
-          const int rp = (d - a.rope_offset) / 2;
-          rot[p] = d >= a.rope_offset && rp < f.n_pairs;
-          if (rot[p]) rope_sincos(pos, f.hi[rp], f.lo[rp], &sn[p], &cs[p]);
-        }
-        const __nv_bfloat16* qb =
-            static_cast<const __nv_bfloat16*>(a.q) + (static_cast<long long>(w.b) * a.n_h + w.h0) * D + hl * 8;
+        for (int p = 0; p < 4; ++p)
+          if (in_span) rope_sincos(pos, f.hi[rel / 2 + p], f.lo[rel / 2 + p], &sn[p], &cs[p]);
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           float x[8];
           bf16x8_to_f32(*reinterpret_cast<const uint4*>(qb + h * D), x);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            if (rot[p]) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
+            if (in_span) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
             q2[h][p] = make_float2(x[2 * p] * a.scale_log2, x[2 * p + 1] * a.scale_log2);
           }
+        }
+      } else {
+        // split halves: dim rel + e pairs with rel + e +- n_pairs, held by the lane
+        // n_pairs / 8 chunks away (n_pairs % 8 == 0); every lane joins the shuffles
+        const bool first = rel < f.n_pairs;
+        const int jb = first ? rel : rel - f.n_pairs;  // pair index of element 0
+        const int partner = (lane & 16) | (in_span ? (first ? hl + f.n_pairs / 8 : hl - f.n_pairs / 8) : hl);
+        float sn[8], cs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (in_span) rope_sincos(pos, f.hi[jb + e], f.lo[jb + e], &sn[e], &cs[e]);
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          float x[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(qb + h * D), x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float y = __shfl_sync(0xffffffffu, x[e], partner);
+            if (in_span) {
+              float lo = first ? x[e] : y, hi = first ? y : x[e];
+              rotate_pair(lo, hi, sn[e], cs[e]);
+              x[e] = first ? lo : hi;
+            }
+          }
+#pragma unroll
+          for (int p = 0; p < 4; ++p) q2[h][p] = make_float2(x[2 * p] * a.scale_log2, x[2 * p + 1] * a.scale_log2);
         }
       }
       float2 o2[HG][4];

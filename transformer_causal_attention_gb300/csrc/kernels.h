@@ -16,7 +16,7 @@ struct PrefillArgs {
   const void* v;
   void* out;
   float* lse;  // nullable
-  int B, S, n_h, n_kv, D;  // S = query rows per sequence
+  int B, S, n_h, n_kv, D;  // S = query rows per sequence; D = head dim of q and k
   float scale_log2;  // score multiplier times log2(e)
   int causal;
   unsigned int* status;
@@ -26,6 +26,8 @@ struct PrefillArgs {
   int kv_rows;       // rows per sequence in the K/V buffers (S for a prompt, max_len for a cache)
   int window;        // > 0: a query at position p sees keys n with p - n < window ...
   int n_sink;        // ... plus the first n_sink keys (attention sinks); window 0: no window
+  int D_v;           // head dim of v and out
+  int rope_offset;   // first rotated dim of q and k (the span holds 2 * n_pairs dims)
 };
 
 struct DecodeArgs {
@@ -89,7 +91,7 @@ struct KvAppendArgs {
 // the number of kernels it enqueued to *launches.
 cudaError_t launch_prefill_simt(const PrefillArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
                                 int* launches);
-bool prefill_tc_supported(int D, bool bf16);
+bool prefill_tc_supported(int D_qk, int D_v, bool bf16);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps,
                               int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_rope(const RopeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches);

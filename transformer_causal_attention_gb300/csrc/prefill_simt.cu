@@ -43,21 +43,33 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(PrefillArgs a, RopeFr
   const int g = h / (a.n_h / a.n_kv);
 
   const T* qrow = static_cast<const T*>(a.q) + ((static_cast<long long>(b) * a.S + m) * a.n_h + h) * D;
-  for (int i = lane; i < D / 2; i += 32) {
-    float x0 = to_f32(qrow[2 * i]), x1 = to_f32(qrow[2 * i + 1]);
-    if (f.n_pairs) {
+  for (int p = lane; p < D / 2; p += 32) {
+    // pair slot p covers dims (2p, 2p + 1), except inside the rotated span
+    // (rope_offset is even) where it is rotation pair j = p - rope_offset / 2
+    const int j = p - a.rope_offset / 2;
+    const bool rot = j >= 0 && j < f.n_pairs;
+    int2 d = make_int2(2 * p, 2 * p + 1);
+    if (rot) {
+      d = rope_pair_dims(f, j);
+      d.x += a.rope_offset;
+      d.y += a.rope_offset;
+    }
+    float x0 = to_f32(qrow[d.x]), x1 = to_f32(qrow[d.y]);
+    if (rot) {
       float s, c;
-      rope_sincos(a.q_offset + m, f.hi[i], f.lo[i], &s, &c);
+      rope_sincos(a.q_offset + m, f.hi[j], f.lo[j], &s, &c);
       rotate_pair(x0, x1, s, c);
     }
-    q_s[warp][2 * i] = x0 * a.scale_log2;
-    q_s[warp][2 * i + 1] = x1 * a.scale_log2;
+    q_s[warp][d.x] = x0 * a.scale_log2;
+    q_s[warp][d.y] = x1 * a.scale_log2;
   }
   __syncwarp();
 
-  const long long row_stride = static_cast<long long>(a.n_kv) * D;  // between consecutive keys
+  const int Dv = a.D_v;
+  const long long row_stride = static_cast<long long>(a.n_kv) * D;     // between consecutive keys
+  const long long vrow_stride = static_cast<long long>(a.n_kv) * Dv;   // between consecutive values
   const T* kbase = static_cast<const T*>(a.k) + (static_cast<long long>(b) * a.kv_rows * a.n_kv + g) * D;
-  const T* vbase = static_cast<const T*>(a.v) + (static_cast<long long>(b) * a.kv_rows * a.n_kv + g) * D;
+  const T* vbase = static_cast<const T*>(a.v) + (static_cast<long long>(b) * a.kv_rows * a.n_kv + g) * Dv;
   constexpr int NT = DMAX / 32;
   float acc[NT];
 #pragma unroll
@@ -91,23 +103,23 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(PrefillArgs a, RopeFr
       const int cnt = min(32, r_hi - n0);
       for (int j = 0; j < cnt; ++j) {
         const float pj = __shfl_sync(0xffffffffu, p, j);
-        const T* vr = vbase + (n0 + j) * row_stride;
+        const T* vr = vbase + (n0 + j) * vrow_stride;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int d = lane + 32 * t;
-          if (d < D) acc[t] = fmaf(pj, to_f32(vr[d]), acc[t]);
+          if (d < Dv) acc[t] = fmaf(pj, to_f32(vr[d]), acc[t]);
         }
       }
       m_run = m_new;
     }
   }
 
-  T* orow = static_cast<T*>(a.out) + ((static_cast<long long>(b) * a.S + m) * a.n_h + h) * D;
+  T* orow = static_cast<T*>(a.out) + ((static_cast<long long>(b) * a.S + m) * a.n_h + h) * Dv;
   const float inv_l = 1.f / l;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int d = lane + 32 * t;
-    if (d < D) orow[d] = from_f32<T>(acc[t] * inv_l);
+    if (d < Dv) orow[d] = from_f32<T>(acc[t] * inv_l);
   }
   if (a.lse != nullptr && lane == 0)
     a.lse[(static_cast<long long>(b) * a.n_h + h) * a.S + m] = (m_run + log2f(l)) * 0.69314718055994530942f;
@@ -117,11 +129,12 @@ template <typename T>
 cudaError_t launch_t(const PrefillArgs& a, const RopeFreq& f, cudaStream_t st) {
   const long long rows = static_cast<long long>(a.B) * a.n_h * a.S;
   const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
-  if (a.D <= 32)
+  const int dmax = a.D > a.D_v ? a.D : a.D_v;  // the query row and the output row share DMAX
+  if (dmax <= 32)
     prefill_simt_kernel<T, 32><<<blocks, 128, 0, st>>>(a, f);
-  else if (a.D <= 64)
+  else if (dmax <= 64)
     prefill_simt_kernel<T, 64><<<blocks, 128, 0, st>>>(a, f);
-  else if (a.D <= 128)
+  else if (dmax <= 128)
     prefill_simt_kernel<T, 128><<<blocks, 128, 0, st>>>(a, f);
   else
     prefill_simt_kernel<T, 256><<<blocks, 128, 0, st>>>(a, f);

@@ -9,11 +9,13 @@
 // the diagonal tile applies the -inf mask.
 //
 // GB300 mapping (one persistent CTA per SM, 384 threads):
-//   warp 0      TMA producer: Q tiles once per work item, K/V tiles through a
-//               ring of shared-memory stages (128-byte swizzle).
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//               S_t = Q_t K_j^T (A, B from shared memory) and O_t += P_t V_j
-//               (P read from TMEM, V from shared memory as an MN-major operand).
+//   warps 0, 2  TMA producers: K tiles (warp 0), and the Q tiles of each work
+//               item followed by its V tiles (warp 2), through rings of
+//               shared-memory stages (128-byte swizzle).
+//   warps 1, 3  MMA issuers, one lane per Q tile: S_t = Q_t K_j^T (A, B from
+//               shared memory) and O_t += P_t V_j (P read from TMEM, V from
+//               shared memory as an MN-major operand).  Warp 1 also allocates
+//               the 512 TMEM columns.
 //   warps 4-7   softmax warpgroup of Q tile 0, warps 8-11 of Q tile 1: each thread
 //               owns one query row (TMEM lane), so row max / row sum need no
 //               shuffles.  P is written back over S in TMEM as bf16.  The output
@@ -24,9 +26,13 @@
 //   Items are taken heaviest-first (latest Q tiles see the most keys).
 // RoPE: the query tile is rotated in shared memory right after its TMA load
 // (once per item); keys arrive already rotated (written once by the rope pass).
+// Head dims: (64, 64), (128, 128) and the MLA prefill shape D_qk = 192 (128
+// content dims + 64 rotated dims), D_v = 128 ("Transformer 与 LLM" slide 06).
 // TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1,
-//               [256, 256+D) O of tile 0, [256+D, 256+2D) O of tile 1.
+//               [256, 256+D_v) O of tile 0, [256+D_v, 256+2D_v) O of tile 1.
 #include <math.h>
+
+#include <atomic>
 
 #include "kernels.h"
 
@@ -38,26 +44,47 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// Register split.  The launch holds 168 registers per thread (384 threads, one
+// CTA per SM); the control warpgroup needs fewer, so it drops to kRegsCtl and
+// the two softmax warpgroups rise to kRegsSoftmax: a row of 128 fp32 scores
+// plus the online-softmax state then fits without spilling.  setmaxnreg.inc
+// waits until the pool has the registers, so the split must fit the pool; the
+// launcher checks the compiled register count against it before launching.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtl = 136, kRegsSoftmax = 184;
+constexpr int kRegsNeeded = 4 * 32 * kRegsCtl + 8 * 32 * kRegsSoftmax;
+static_assert(kRegsNeeded <= kThreads * kLaunchRegs, "register split exceeds the launch's pool");
+
+// Head dims DQK (q, k) and DV (v, out).  Every tile is stored as 64-element
+// (128-byte) column blocks of 128 rows with the 128-byte swizzle.  Shared
+// memory holds both Q tiles, kKStages K tiles and kVStages V tiles; with
+// DQK = 192 (the MLA prefill shape) only one V stage fits beside two K stages.
+template <int DQK, int DV>
 struct Cfg {
-  static constexpr int kDBlocks = D / 64;         // 64-element (128-byte) column blocks
-  static constexpr int kTileBytes = BM * D * 2;   // one bf16 Q, K or V tile
+  static_assert(BM == BN, "Q, K and V tiles share one row count");
+  static constexpr int kQBlocks = DQK / 64;       // column blocks of a Q or K tile
+  static constexpr int kVBlocks = DV / 64;        // column blocks of a V tile
+  static constexpr int kQKTileBytes = BM * DQK * 2;
+  static constexpr int kVTileBytes = BN * DV * 2;
   static constexpr int kBlockBytes = BM * 128;    // one column block of a tile
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kKStages = DQK == 64 ? 3 : 2;
+  static constexpr int kVStages = DQK == 64 ? 3 : (DQK == 128 ? 2 : 1);
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kKOff = kQOff + 2 * kQKTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kQKTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kVTileBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t kOCol0 = 256;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kOCol0 = 256;         // S of the two tiles in columns [0, 256)
+  static_assert(kOCol0 + 2 * DV <= 512, "TMEM columns");
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, false);
-  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, true);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, true);
 };
 
 struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
-  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];  // up to 3 stages
   uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
@@ -136,12 +163,60 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+// Rotate the span [rope_offset, rope_offset + 2 * n_pairs) of query row r
+// (position pos) of a Q tile in place.  The tile is stored as column blocks of
+// 128 rows x 128 bytes with the 128-byte swizzle: the 16-byte chunk c of row r
+// sits at chunk (c & 7) ^ (r & 7) of block c >> 3.  rope_offset is a multiple
+// of 8 (whole chunks).  Kept out of line: it runs once per tile row, and inlined
+// it costs the softmax loop registers.
+template <int DQK>
+__device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope_offset, const RopeFreq& f) {
+  constexpr int kBlockBytes = BM * 128;
+  auto chunk = [&](int c) -> uint8_t* { return row + (c >> 3) * kBlockBytes + (((c & 7) ^ (r & 7)) << 4); };
+  const int c0 = rope_offset / 8;
+  if (f.half) {
+    // pair j = span dims (j, j + n_pairs): chunk c0 + i holds the first members of
+    // pairs 8i..8i+7, chunk c0 + i + n_pairs / 8 their second members
+    const int hc = f.n_pairs / 8;
+#pragma unroll 1
+    for (int i = 0; i < hc; ++i) {
+      uint4* p0 = reinterpret_cast<uint4*>(chunk(c0 + i));
+      uint4* p1 = reinterpret_cast<uint4*>(chunk(c0 + i + hc));
+      float x0[8], x1[8];
+      bf16x8_to_f32(*p0, x0);
+      bf16x8_to_f32(*p1, x1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float sn, cs;
+        rope_sincos(pos, f.hi[i * 8 + e], f.lo[i * 8 + e], &sn, &cs);
+        rotate_pair(x0[e], x1[e], sn, cs);
+      }
+      *p0 = f32_to_bf16x8(x0);
+      *p1 = f32_to_bf16x8(x1);
+    }
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < f.n_pairs / 4; ++i) {
+      uint4* p = reinterpret_cast<uint4*>(chunk(c0 + i));
+      float x[8];
+      bf16x8_to_f32(*p, x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float sn, cs;
+        rope_sincos(pos, f.hi[i * 4 + e], f.lo[i * 4 + e], &sn, &cs);
+        rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
+      }
+      *p = f32_to_bf16x8(x);
+    }
+  }
+}
+
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<D>;
+  using C = Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
@@ -162,13 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_empty[t], 128);
     }
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 2);  // released by both MMA issuers
     }
-    mbar_init(&bars->fin, 1);
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 2);
+    }
+    mbar_init(&bars->fin, 2);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -187,160 +264,168 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, a.status, a.wait_limit_ns};
 
-  // Q tile t lives at smem + kQOff + t * kTileBytes (arithmetic, not an array:
+  // Q tile t lives at smem + kQOff + t * kQKTileBytes (arithmetic, not an array:
   // runtime-indexed local arrays would live in local memory)
-  auto q_smem = [&](int t) { return smem + C::kQOff + t * C::kTileBytes; };
+  auto q_smem = [&](int t) { return smem + C::kQOff + t * C::kQKTileBytes; };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
-      uint32_t k_issued = 0, v_issued = 0;  // bit s: stage s has had a load issued
-      uint32_t k_last_ph = 0, v_last_ph = 0;  // bit s: phase parity of that load
-      uint32_t q_issued = 0;
-      uint32_t it = 0;
-      for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
-        const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
-        for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait(&bars->q_empty[t], (it & 1) ^ 1, wc)) goto producer_done;
-          mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
-          for (int db = 0; db < C::kDBlocks; ++db)
-            tma_load_4d(q_smem(t) + db * C::kBlockBytes, &tm_q, &bars->q_full[t], db * 64, itm.h,
-                        (itm.qt0 + t) * BM, itm.b);
-          q_issued = it + 1;
-        }
-        for (int v = 0; v < itm.n_load; ++v) {
-          const int j = itm.load_at(v);
-          if (!mbar_wait(&bars->k_empty[kst], kph ^ 1, wc)) goto producer_done;
-          mbar_arrive_expect_tx(&bars->k_full[kst], C::kTileBytes);
-          uint8_t* kdst = smem + C::kKOff + kst * C::kTileBytes;
-          for (int db = 0; db < C::kDBlocks; ++db)
-            tma_load_4d(kdst + db * C::kBlockBytes, &tm_k, &bars->k_full[kst], db * 64, itm.g, j * BN, itm.b);
-          k_issued |= 1u << kst;
-          k_last_ph = (k_last_ph & ~(1u << kst)) | (kph << kst);
-          if (++kst == C::kStages) { kst = 0; kph ^= 1; }
-
-          if (!mbar_wait(&bars->v_empty[vst], vph ^ 1, wc)) goto producer_done;
-          mbar_arrive_expect_tx(&bars->v_full[vst], C::kTileBytes);
-          uint8_t* vdst = smem + C::kVOff + vst * C::kTileBytes;
-          for (int db = 0; db < C::kDBlocks; ++db)
-            tma_load_4d(vdst + db * C::kBlockBytes, &tm_v, &bars->v_full[vst], db * 64, itm.g, j * BN, itm.b);
-          v_issued |= 1u << vst;
-          v_last_ph = (v_last_ph & ~(1u << vst)) | (vph << vst);
-          if (++vst == C::kStages) { vst = 0; vph ^= 1; }
-        }
-      }
-    producer_done:
-      if (bars->abort_flag) {  // let every copy in flight land before shared memory goes away
-        for (int s = 0; s < C::kStages; ++s) {
-          if (k_issued & (1u << s)) drain_wait(&bars->k_full[s], (k_last_ph >> s) & 1, a.wait_limit_ns);
-          if (v_issued & (1u << s)) drain_wait(&bars->v_full[s], (v_last_ph >> s) & 1, a.wait_limit_ns);
-        }
-        if (q_issued)
-          for (int t = 0; t < 2; ++t) drain_wait(&bars->q_full[t], (q_issued - 1) & 1, a.wait_limit_ns);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t q_addr0 = smem_u32(q_smem(0));
-      uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
-      uint32_t pph0 = 0u, pph1 = 0u;
-      uint32_t it = 0;
-      auto issue_qk = [&](int t, uint32_t stage) {
-        const uint32_t kbase = smem_u32(smem + C::kKOff + stage * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * 128u, sdesc_sw128(q_addr0 + t * C::kTileBytes + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
-        const uint32_t vbase = smem_u32(smem + C::kVOff + stage * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem + C::kOCol0 + t * D, tmem + t * 128u + kk * 8,
-                 sdesc_sw128(vbase + kk * 16 * 128, C::kBlockBytes, 1024), C::kIdescPV,
-                 (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-      for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
-        const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
-        // Loaded tile v feeds Q tile t when t's range has it.  Per loaded tile:
-        // P V of every member tile, then QK of the next loaded tile for its
-        // members (so S_t is reused only after P_t was consumed; MMAs run in order).
-        bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
-        if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
-        {
-          const int j0 = itm.load_at(0);
-          for (int t = 0; t < 2; ++t) {
-            if (!(t ? itm.r1 : itm.r0).has(j0)) continue;
-            if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
-            (t ? q_seen1 : q_seen0) = true;
-            tc_fence_after();
-            issue_qk(t, kst);
-            mma_commit(&bars->s_full[t]);
+  if (warp < 4) {
+    // control warpgroup: TMA producers (warps 0, 2) and the MMA issuers
+    // (warps 1, 3); its registers go to the softmax warpgroups
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0 || warp == 2) {
+      // ------------------------------------------------------------ TMA producers
+      // Two independent rings, one lane each: warp 0 loads K tiles; warp 2 the
+      // two Q tiles of each work item, then its V tiles.  The K ring runs ahead
+      // into the next item while the Q loads wait for the current epilogues.
+      if (lane == 0) {
+        const bool is_v = warp == 2;
+        const int n_stages = is_v ? C::kVStages : C::kKStages;
+        const int tile_bytes = is_v ? C::kVTileBytes : C::kQKTileBytes;
+        const int n_blocks = is_v ? C::kVBlocks : C::kQBlocks;
+        uint8_t* const ring = smem + (is_v ? C::kVOff : C::kKOff);
+        uint64_t* const full = is_v ? bars->v_full : bars->k_full;
+        uint64_t* const empty = is_v ? bars->v_empty : bars->k_empty;
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+        uint32_t st = 0, ph = 0;
+        uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
+        uint32_t q_issued = 0, it = 0;
+        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
+          const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
+          if (is_v) {
+            for (int t = 0; t < 2; ++t) {
+              if (!mbar_wait(&bars->q_empty[t], (it & 1) ^ 1, wc)) goto load_done;
+              mbar_arrive_expect_tx(&bars->q_full[t], C::kQKTileBytes);
+              for (int db = 0; db < C::kQBlocks; ++db)
+                tma_load_4d(q_smem(t) + db * C::kBlockBytes, &tm_q, &bars->q_full[t], db * 64, itm.h,
+                            (itm.qt0 + t) * BM, itm.b);
+              q_issued = it + 1;
+            }
+          }
+          for (int v = 0; v < itm.n_load; ++v) {
+            const int j = itm.load_at(v);
+            if (!mbar_wait(&empty[st], ph ^ 1, wc)) goto load_done;
+            mbar_arrive_expect_tx(&full[st], tile_bytes);
+            uint8_t* dst = ring + st * tile_bytes;
+            for (int db = 0; db < n_blocks; ++db)
+              tma_load_4d(dst + db * C::kBlockBytes, map, &full[st], db * 64, itm.g, j * BN, itm.b);
+            issued |= 1u << st;
+            last_ph = (last_ph & ~(1u << st)) | (ph << st);
+            if (++st == static_cast<uint32_t>(n_stages)) { st = 0; ph ^= 1; }
           }
         }
-        mma_commit(&bars->k_empty[kst]);
-        if (++kst == C::kStages) { kst = 0; kph ^= 1; }
-        for (int v = 0; v < itm.n_load; ++v) {
-          const int j = itm.load_at(v);
-          const bool next = v + 1 < itm.n_load;
-          const int jn = next ? itm.load_at(v + 1) : -1;
-          if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
-          bool k_ready = false;
-          for (int t = 0; t < 2; ++t) {
-            const TileRange& r = t ? itm.r1 : itm.r0;
-            if (r.has(j)) {
-              if (!mbar_wait(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
-              if (t) pph1 ^= 1; else pph0 ^= 1;
-              const bool seen = t ? pv_seen1 : pv_seen0;
-              if (!seen && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
-              tc_fence_after();
-              issue_pv(t, vst, seen);
-              if (t) pv_seen1 = true; else pv_seen0 = true;
-              if (j == r.jh) mma_commit(&bars->o_done[t]);
-            }
-            if (t == 1) {
-              mma_commit(&bars->v_empty[vst]);
-              if (++vst == C::kStages) { vst = 0; vph ^= 1; }
-            }
-            if (next && r.has(jn)) {
-              if (!k_ready) {
-                if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
-                k_ready = true;
+      load_done:
+        if (bars->abort_flag) {  // let every copy in flight land before shared memory goes away
+          for (int s2 = 0; s2 < n_stages; ++s2)
+            if (issued & (1u << s2)) drain_wait(&full[s2], (last_ph >> s2) & 1, a.wait_limit_ns);
+          if (q_issued)
+            for (int t = 0; t < 2; ++t) drain_wait(&bars->q_full[t], (q_issued - 1) & 1, a.wait_limit_ns);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ MMA issuers
+      // One issuing lane per Q tile (warp 1: tile 0, warp 3: tile 1), so that
+      // the waits and bookkeeping of one tile overlap the other tile's MMAs
+      // (a tcgen05.mma is accepted only as the tensor pipe frees a slot, so a
+      // single issuer serialises every wait with the pipe).  Per member key tile
+      // m_i of its range: P V(m_{i-1}) then Q K(m_i), back to back (QK reuses
+      // the S/P columns the P V reads, so the two stay ordered in one thread).
+      // Both issuers walk every loaded tile of both rings, releasing each stage
+      // once (empty barriers count two arrivals), after its full barrier; a
+      // pending P V is issued before passing a tile the Q tile does not need, so
+      // no issuer holds a V stage while it waits for a later one.
+      if (lane == 0) {
+        const int t = warp == 1 ? 0 : 1;
+        const uint64_t q_desc = sdesc_sw128(smem_u32(q_smem(t)), 16, 1024);
+        const uint64_t k_desc0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+        const uint64_t v_desc0 = sdesc_sw128(smem_u32(smem + C::kVOff), C::kBlockBytes, 1024);
+        const uint32_t s_tm = tmem + t * 128u, o_tm = tmem + C::kOCol0 + t * DV;
+        uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph = 0;
+        uint32_t it = 0;
+        // Descriptors advance by adding offsets in 16-byte units to the start-
+        // address field (shared-memory addresses stay below 256 KB, so the 14-bit
+        // field never carries); the K loops are unrolled.
+        auto issue_qk = [&](uint32_t stage) {
+          const uint64_t b0 = k_desc0 + ((stage * C::kQKTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kBlockBytes + (kk & 3) * 32) >> 4;
+            mma_ss(s_tm, q_desc + off, b0 + off, C::kIdescQK, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_pv = [&](uint32_t stage, bool accumulate) {
+          const uint64_t b0 = v_desc0 + ((stage * C::kVTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(o_tm, s_tm + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        // P V of the pending member tile (its V ring entry is prev_vst / prev_vph)
+        bool have_prev = false, pv_started = false;
+        uint32_t prev_vst = 0, prev_vph = 0;
+        auto issue_pending_pv = [&]() -> bool {
+          if (!mbar_wait(&bars->p_full[t], pph, wc)) return false;
+          pph ^= 1;
+          if (!pv_started && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) return false;
+          if (!mbar_wait(&bars->v_full[prev_vst], prev_vph, wc)) return false;
+          tc_fence_after();
+          issue_pv(prev_vst, pv_started);
+          pv_started = true;
+          mma_commit(&bars->v_empty[prev_vst]);
+          have_prev = false;
+          return true;
+        };
+        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
+          const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
+          const TileRange rng = t ? itm.r1 : itm.r0;
+          bool q_seen = false;
+          pv_started = false;
+          for (int v = 0; v < itm.n_load; ++v) {
+            const bool mine = rng.has(itm.load_at(v));
+            if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
+            if (mine) {
+              // P V of the previous member and Q K of this one, back to back
+              if (have_prev && !issue_pending_pv()) goto mma_done;
+              if (!q_seen) {
+                if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+                q_seen = true;
+                tc_fence_after();
               }
-              const bool qs = t ? q_seen1 : q_seen0;
-              if (!qs && !mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
-              if (t) q_seen1 = true; else q_seen0 = true;
-              tc_fence_after();
-              issue_qk(t, kst);
+              issue_qk(kst);
               mma_commit(&bars->s_full[t]);
+              mma_commit(&bars->k_empty[kst]);
+              have_prev = true;
+              prev_vst = vst;
+              prev_vph = vph;
+            } else {
+              // a tile only the other Q tile needs: finish the pending P V (so no
+              // V stage stays held), then pass both ring entries on
+              if (have_prev && !issue_pending_pv()) goto mma_done;
+              mbar_arrive(&bars->k_empty[kst]);
+              if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+              mbar_arrive(&bars->v_empty[vst]);
             }
+            if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+            if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
           }
-          if (next) {
-            mma_commit(&bars->k_empty[kst]);
-            if (++kst == C::kStages) { kst = 0; kph ^= 1; }
-          }
+          if (have_prev && !issue_pending_pv()) goto mma_done;  // the last member tile
+          mma_commit(&bars->o_done[t]);
         }
+      mma_done:
+        // every MMA this lane issued completes before TMEM is released
+        mma_commit(&bars->fin);
+        drain_wait(&bars->fin, 0, a.wait_limit_ns);
       }
-    mma_done:
-      // every MMA issued so far completes before TMEM is released
-      mma_commit(&bars->fin);
-      drain_wait(&bars->fin, 0, a.wait_limit_ns);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= 4) {
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax warpgroups
     const int t = (warp - 4) >> 2;     // Q tile of this warpgroup
     const int quad = warp & 3;         // TMEM lane quadrant
     const int r = quad * 32 + lane;    // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + (t ? 128u : 0u);
-    const uint32_t o_addr = tmem + lane_off + C::kOCol0 + (t ? D : 0);
+    const uint32_t o_addr = tmem + lane_off + C::kOCol0 + (t ? DV : 0);
     uint32_t sph = 0;
     uint32_t it = 0;
     for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
@@ -352,22 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = a.q_offset + m;  // its absolute position
       if (!warp_wait(&bars->q_full[t], it & 1, wc)) break;
       if (f.n_pairs) {
-        // rotate this thread's query row in place (swizzled layout: the 16-byte
-        // chunk c of row r sits at chunk c ^ (r & 7) of the row's 128-byte line)
-        uint8_t* row = q_smem(t) + r * 128;
-#pragma unroll 1
-        for (int c = 0; c < D / 8; ++c) {
-          uint4* p = reinterpret_cast<uint4*>(row + (c >> 3) * C::kBlockBytes + (((c & 7) ^ (r & 7)) << 4));
-          float x[8];
-          bf16x8_to_f32(*p, x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float sn, cs;
-            rope_sincos(pos, f.hi[c * 4 + e], f.lo[c * 4 + e], &sn, &cs);
-            rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
-          }
-          *p = f32_to_bf16x8(x);
-        }
+        rotate_q_row<DQK>(q_smem(t) + r * 128, r, pos, a.rope_offset, f);
         fence_proxy_async_smem();
       }
       mbar_arrive(&bars->q_ready[t]);
@@ -405,18 +475,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (key0 + c >= a.S_k) s[c] = -INFINITY;
         }
-        // row maximum: 8 independent chains, then a tree (a single chain of 127
-        // dependent max operations would dominate the warp's latency)
+        // row maximum: 8 independent chains of three-input max (two new columns
+        // per instruction), then a tree; a single chain of 127 dependent max
+        // operations would dominate the warp's latency
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = s[i];
+        static_assert((BN - 8) % 16 == 8, "chains take 16 columns per round plus one round of 8");
 #pragma unroll
-        for (int c = 8; c < BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+        for (int c = 8; c + 16 <= BN; c += 16)
 #pragma unroll
-        for (int w2 = 4; w2 > 0; w2 >>= 1)
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
 #pragma unroll
-          for (int i = 0; i < w2; ++i) m8[i] = fmaxf(m8[i], m8[i + w2]);
-        const float mx = m8[0] * a.scale_log2;
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BN - 8 + i]);
+        const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7])) *
+                         a.scale_log2;
         // Move to a new reference maximum only when the row maximum grew by more
         // than the threshold; O and l are then scaled by alpha = 2^(m_old - m_new).
         const bool need = mx > m_run + kRescaleThreshold;
@@ -452,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp rescales when any of its rows needs it (alpha is 1 for the others).
         if (__any_sync(0xffffffffu, need && i > 0)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             uint32_t orow[32];
             tmem_ld32(o_addr + c * 32, orow);
             tmem_wait_ld();
@@ -474,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = 1.f / l_run;
       const bool store = m < a.S;
       __nv_bfloat16* orow_g = static_cast<__nv_bfloat16*>(a.out) +
-                              ((static_cast<long long>(itm.b) * a.S + m) * a.n_h + itm.h) * D;
+                              ((static_cast<long long>(itm.b) * a.S + m) * a.n_h + itm.h) * DV;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t orow[32];
         tmem_ld32(o_addr + c * 32, orow);
         tmem_wait_ld();
@@ -509,7 +582,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool prefill_tc_supported(int D, bool bf16) { return bf16 && (D == 64 || D == 128); }
+namespace {
+// Per head-dim pair, one bit per device that has been prepared.
+std::atomic<unsigned> g_ready[3];
+
+// Opt in to the kernel's shared memory and check, once per process and device,
+// that the compiled kernel holds enough registers per thread for its register
+// split (a split above the pool would leave setmaxnreg.inc waiting forever).
+template <typename K>
+cudaError_t prepare(K kernel, int smem_bytes, std::atomic<unsigned>* ready) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (ready->load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
+  if (static_cast<long long>(fa.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
+    return e;
+  ready->fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+template <int DQK, int DV>
+cudaError_t launch(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int grid, cudaStream_t st,
+                   std::atomic<unsigned>* ready) {
+  auto k = prefill_tc_kernel<DQK, DV>;
+  const cudaError_t e = prepare(k, Cfg<DQK, DV>::kSmemBytes, ready);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, Cfg<DQK, DV>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
+  return cudaGetLastError();
+}
+}  // namespace
+
+bool prefill_tc_supported(int D_qk, int D_v, bool bf16) {
+  return bf16 && ((D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128) || (D_qk == 192 && D_v == 128));
+}
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
                               cudaStream_t st, int* launches) {
@@ -517,19 +626,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const 
   const long long n_items = static_cast<long long>(a.B) * a.n_h * ((n_qt + 1) / 2);
   const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
   cudaError_t e;
-  if (a.D == 64) {
-    auto k = prefill_tc_kernel<64>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, Cfg<64>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
-  } else {
-    auto k = prefill_tc_kernel<128>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, Cfg<128>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
-  }
+  if (a.D == 64)
+    e = launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
+  else if (a.D == 128)
+    e = launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
+  else
+    e = launch<192, 128>(a, rope, maps, grid, st, &g_ready[2]);
   *launches += 1;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace attn

@@ -1,17 +1,73 @@
 // rope.cu - standalone rotary position embedding of [B, S, n_heads, D] rows.
 //
-// Rotates the pairs (2i, 2i+1) of the span [rope_offset, rope_offset + rope_dims)
-// by pos * theta_i ("Transformer架构从Attention到DecoderBlock" §8.3).  This is the
+// Rotates the pairs of the span [rope_offset, rope_offset + rope_dims) by
+// pos * theta_i ("Transformer架构从Attention到DecoderBlock" §8.3): pairs
+// (2i, 2i+1), or (j, j + rope_dims/2) in the split-halves layout.  This is the
 // pass that writes rotated keys (the KV-cache form, "Transformer架构完全深度解析"
 // §7) before the prefill kernel reads them.
 //
 // One thread owns a chunk of CH consecutive dims of one token for ALL heads, so
-// the sin/cos of its pairs are computed once and reused n_heads times.  The
-// kernel is bound by HBM bandwidth (read + write once).
+// the sin/cos of its pairs are computed once and reused n_heads times.  In the
+// split-halves layout the thread owning a chunk of the first half also owns the
+// chunk rope_dims/2 later, which holds the other member of each of its pairs.
+// The kernel is bound by HBM bandwidth (read + write once).
 #include "kernels.h"
 
 namespace attn {
 namespace {
+
+template <typename T, int CH>
+__device__ __forceinline__ void load_chunk(const T* p, float* x) {
+  if constexpr (sizeof(T) == 2 && CH == 8) {
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), x);
+  } else {
+#pragma unroll
+    for (int e = 0; e < CH; ++e) x[e] = to_f32(p[e]);
+  }
+}
+
+template <typename T, int CH>
+__device__ __forceinline__ void store_chunk(T* p, const float* x) {
+  if constexpr (sizeof(T) == 2 && CH == 8) {
+    *reinterpret_cast<uint4*>(p) = f32_to_bf16x8(x);
+  } else {
+#pragma unroll
+    for (int e = 0; e < CH; ++e) p[e] = from_f32<T>(x[e]);
+  }
+}
+
+// Rotate n_rows rows (stride `stride` elements) of the chunk at span-relative
+// dim `rel` from src to dst at position pos.  The caller skips chunks of the
+// second half in the split-halves layout (their owner is rel - n_pairs).
+template <typename T, int CH>
+__device__ __forceinline__ void rotate_chunk_rows(const T* src, T* dst, long long stride, int n_rows, int rel, int pos,
+                                                  const RopeFreq& f) {
+  if (f.half) {
+    float sn[CH], cs[CH];
+#pragma unroll
+    for (int e = 0; e < CH; ++e) rope_sincos(pos, f.hi[rel + e], f.lo[rel + e], &sn[e], &cs[e]);
+    for (int h = 0; h < n_rows; ++h) {
+      float x0[CH], x1[CH];
+      load_chunk<T, CH>(src + h * stride, x0);
+      load_chunk<T, CH>(src + h * stride + f.n_pairs, x1);
+#pragma unroll
+      for (int e = 0; e < CH; ++e) rotate_pair(x0[e], x1[e], sn[e], cs[e]);
+      store_chunk<T, CH>(dst + h * stride, x0);
+      store_chunk<T, CH>(dst + h * stride + f.n_pairs, x1);
+    }
+  } else {
+    float sn[CH / 2], cs[CH / 2];
+#pragma unroll
+    for (int p = 0; p < CH / 2; ++p) rope_sincos(pos, f.hi[rel / 2 + p], f.lo[rel / 2 + p], &sn[p], &cs[p]);
+    for (int h = 0; h < n_rows; ++h) {
+      float x[CH];
+      load_chunk<T, CH>(src + h * stride, x);
+#pragma unroll
+      for (int p = 0; p < CH / 2; ++p) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
+      store_chunk<T, CH>(dst + h * stride, x);
+    }
+  }
+}
 
 template <typename T, int CH>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq f) {
@@ -25,37 +81,16 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq f) {
     const long long tok = idx / chunks;  // b * S + s
     const int s = static_cast<int>(tok % a.S);
     const int d0 = c * CH;
-    const bool rotated = d0 >= a.rope_offset && d0 < a.rope_offset + a.rope_dims;
-    if (!rotated && in == out) continue;
-    float sn[CH / 2], cs[CH / 2];
-    if (rotated) {
-      const int pair0 = (d0 - a.rope_offset) / 2;
-#pragma unroll
-      for (int p = 0; p < CH / 2; ++p) rope_sincos(a.pos_offset + s, f.hi[pair0 + p], f.lo[pair0 + p], &sn[p], &cs[p]);
-    }
-    const long long row0 = tok * a.n_heads;
-    for (int h = 0; h < a.n_heads; ++h) {
-      const long long off = (row0 + h) * a.D + d0;
-      if constexpr (sizeof(T) == 2 && CH == 8) {
-        uint4 u = *reinterpret_cast<const uint4*>(in + off);
-        if (rotated) {
-          float x[8];
-          bf16x8_to_f32(u, x);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
-          u = f32_to_bf16x8(x);
-        }
-        *reinterpret_cast<uint4*>(out + off) = u;
-      } else {
+    const int rel = d0 - a.rope_offset;
+    const long long off = tok * a.n_heads * a.D + d0;
+    if (rel >= 0 && rel < a.rope_dims) {
+      if (f.half && rel >= f.n_pairs) continue;  // rotated by the owner of its partner chunk
+      rotate_chunk_rows<T, CH>(in + off, out + off, a.D, a.n_heads, rel, a.pos_offset + s, f);
+    } else if (in != out) {
+      for (int h = 0; h < a.n_heads; ++h) {
         float x[CH];
-#pragma unroll
-        for (int e = 0; e < CH; ++e) x[e] = to_f32(in[off + e]);
-        if (rotated) {
-#pragma unroll
-          for (int p = 0; p < CH / 2; ++p) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
-        }
-#pragma unroll
-        for (int e = 0; e < CH; ++e) out[off + e] = from_f32<T>(x[e]);
+        load_chunk<T, CH>(in + off + h * a.D, x);
+        store_chunk<T, CH>(out + off + h * a.D, x);
       }
     }
   }
@@ -80,25 +115,18 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
     const long long slot = static_cast<long long>(b) * a.max_len + pos;
     if (ch < kch) {
       const int d0 = ch * 8;
-      const bool rot = d0 >= a.rope_offset && d0 < a.rope_offset + 2 * f.n_pairs;
-      float sn[4], cs[4];
-      if (rot) {
-        const int p0 = (d0 - a.rope_offset) / 2;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) rope_sincos(pos, f.hi[p0 + p], f.lo[p0 + p], &sn[p], &cs[p]);
-      }
+      const int rel = d0 - a.rope_offset;
       const T* src = static_cast<const T*>(a.k_new) + (bc * a.n_kv) * a.D_qk + d0;
       T* dst = static_cast<T*>(a.kcache) + slot * a.n_kv * a.D_qk + d0;
-      for (int h = 0; h < a.n_kv; ++h) {
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = to_f32(src[h * a.D_qk + e]);
-        if (rot) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
+      if (rel >= 0 && rel < 2 * f.n_pairs) {
+        if (f.half && rel >= f.n_pairs) continue;  // written with its partner chunk
+        rotate_chunk_rows<T, 8>(src, dst, a.D_qk, a.n_kv, rel, pos, f);
+      } else {
+        for (int h = 0; h < a.n_kv; ++h) {
+          float x[8];
+          load_chunk<T, 8>(src + h * a.D_qk, x);
+          store_chunk<T, 8>(dst + h * a.D_qk, x);
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[h * a.D_qk + e] = from_f32<T>(x[e]);
       }
     } else {
       const int d0 = (ch - kch) * 8;

@@ -18,6 +18,10 @@ dataset is involved:
                     ("Transformer 与 LLM" slide 06: about 59 concurrent 8K sequences fit one card)
 * ``mla_decode``  - 32 sequences at 32768 keys, 128 heads sharing one 576-dim latent KV head,
                     V = first 512 latent dims ("Transformer 与 LLM" slide 06)
+* ``mla_prefill`` - DeepSeek-V3-shaped MLA prefill on the non-absorbed path: B=1 S=4096,
+                    128 heads, q/k head dim 192 (128 content + 64 decoupled RoPE dims,
+                    the RoPE part of k shared by all heads), v head dim 128, RoPE base 1e4
+                    on dims [128, 192), scale 1/sqrt(192) ("Transformer 与 LLM" slide 06)
 
 The decode caches are drawn directly as the stored (already rotated) keys:
 rotating i.i.d. N(0, 1) pairs gives i.i.d. N(0, 1) pairs again, so the draw has
@@ -44,6 +48,9 @@ CONFIGS: dict[str, dict] = {
                        n_h=128, n_kv=1, D_qk=576, D_v=512, v_aliases_k=True, dtype="bf16",
                        rope_base=0.0, rope_offset=512, rope_dims=64,
                        scale=1.0 / math.sqrt(192)),
+    "mla_prefill": dict(kind="prefill", B=1, S=4096, n_h=128, n_kv=128, D_qk=192, D_v=128, dtype="bf16",
+                        rope_base=10000.0, rope_offset=128, rope_dims=64, scale=1.0 / math.sqrt(192),
+                        causal=True),
 }
 
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -77,6 +84,21 @@ def prefill_inputs(cfg: dict, seed: int = 0):
     q = _randn((B, S, n_h, D), g, dt)
     k = _randn((B, S, n_kv, D), g, dt)
     v = _randn((B, S, n_kv, D), g, dt)
+    return q, k, v
+
+
+def mla_prefill_inputs(cfg: dict, seed: int = 0):
+    """(q, k, v) on the CPU: q, k [B,S,n_h,D_qk], v [B,S,n_h,D_v].  The last
+    rope_dims dims of k are one draw per token copied to every head (the shared
+    k^R of MLA); everything else is i.i.d. N(0, 1).  Draw order q, k, k^R, v."""
+    g = torch.Generator().manual_seed(seed)
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    B, S, n_h, D_qk, D_v, r = cfg["B"], cfg["S"], cfg["n_h"], cfg["D_qk"], cfg["D_v"], cfg["rope_dims"]
+    q = _randn((B, S, n_h, D_qk), g, dt)
+    k = _randn((B, S, n_h, D_qk), g, dt)
+    k_r = _randn((B, S, 1, r), g, dt)
+    k[..., D_qk - r:] = k_r
+    v = _randn((B, S, n_h, D_v), g, dt)
     return q, k, v
 
 
@@ -120,10 +142,12 @@ def mla_factors(B: int, n_h: int, L: int, seed: int = 0, d_c: int = 128, d_r: in
     return q_c, q_r, c_kv, k_r, w_uk, w_uv
 
 
-def causal_flops(B: int, S: int, n_h: int, D_h: int) -> float:
+def causal_flops(B: int, S: int, n_h: int, D_h: int, D_v: int | None = None) -> float:
     """Causal attention FLOPs as the benchmark counts them: the dense count
-    4 * B * n_h * S^2 * D_h (two matmuls of 2*S^2*D_h each per head), halved."""
-    return 4.0 * B * n_h * S * S * D_h / 2.0
+    2 * B * n_h * S^2 * (D_h + D_v) (Q K^T plus P V; 4 B n_h S^2 D_h when
+    D_v = D_h), halved."""
+    D_v = D_h if D_v is None else D_v
+    return 2.0 * B * n_h * S * S * (D_h + D_v) / 2.0
 
 
 def decode_bytes(cfg: dict, seqlens) -> float:
