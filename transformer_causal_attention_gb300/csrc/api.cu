@@ -441,7 +441,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   const bool chunked_rope = !rope || (rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0);
   const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, bf16) &&
                        decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, bf16) &&
-                       chunked_rope && (!rope || rope_offset >= 384);
+                       chunked_rope && (!rope || rope_offset >= kMlaQTmemDims);
   if (use_mla) {
     ns = decode_mla_pairs(dev.sms);  // the kernel runs 2 CTAs per pair
     chunk = 0;
@@ -458,7 +458,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
     CUtensorMap maps[2];
     const unsigned long long row = static_cast<unsigned long long>(D_qk) * 2;
     if (!make_map3(&maps[0], q, D_qk, n_h, B, row, row * n_h, 128) ||
-        !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, 32))
+        !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, kMlaTileKeys))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);
   } else if (window == 0 && chunked_rope && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {

@@ -36,26 +36,29 @@ constexpr int NH = 128;          // query heads (MMA M)
 constexpr int DQK = 576;         // latent + rotary dims
 constexpr int DV = 512;          // value dims
 constexpr int DVH = 256;         // value dims per CTA of a pair
-constexpr int BK = 32;           // keys per tile (MMA N of the score tile)
-constexpr int kStages = 4;
+constexpr int BK = kMlaTileKeys;  // keys per tile (MMA N of the score tile)
+constexpr int kStages = BK == 32 ? 4 : 2;
 constexpr int kThreads = 256;
 constexpr int kBlocks = DQK / 64;                  // 9 column blocks of 64 dims
-constexpr int kQTmemDims = 384;                    // query dims [0, 384) live in TMEM (A operand)
+constexpr int kQTmemDims = kMlaQTmemDims;          // query dims [0, kQTmemDims) live in TMEM (A operand)
 constexpr int kQSmemBlocks = (DQK - kQTmemDims) / 64;  // dims [384, 576) in shared memory: 3 blocks
 constexpr int kQBlockBytes = NH * 128;             // 16 KB
 constexpr int kQSmemBytes = kQSmemBlocks * kQBlockBytes;  // 48 KB
 constexpr int kKBlockBytes = BK * 128;             // 4 KB
 constexpr int kTileBytes = kBlocks * kKBlockBytes; // 36 KB
-constexpr int kMaxB = 1024;
+constexpr int kMaxB = BK == 32 ? 1024 : 256;  // the key prefix sums of the batch live in shared memory
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQSmemBytes;
 constexpr int kPrefOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kPrefOff + (kMaxB + 1) * 4 + 60;
 constexpr int kSmemBytes = kBarOff + 160 + 1024;
-// TMEM columns: S/P buffer b at [32 b, 32 b + 32), O_half at [64, 320), Q dims [0, 384) at [320, 512)
-__device__ __forceinline__ uint32_t s_col(uint32_t b) { return b * 32u; }
-constexpr uint32_t kOCol = 64u;
-constexpr uint32_t kQCol = 320u;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// TMEM columns: S/P buffer b at [BK b, BK b + BK), O_half at [2 BK, 2 BK + 256), then the query dims
+// [0, kQTmemDims) as bf16 pairs
+__device__ __forceinline__ uint32_t s_col(uint32_t b) { return b * BK; }
+constexpr uint32_t kOCol = 2 * BK;
+constexpr uint32_t kQCol = kOCol + DVH;
+static_assert(kQCol + kQTmemDims / 2 <= 512, "TMEM columns");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(NH, BK, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(NH, DVH, true);
 constexpr float kRescaleThreshold = 8.0f;
@@ -413,16 +416,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1u << sbuf;
         tc_fence_after();
         uint32_t sr[BK];
-        tmem_ld32(tmem + lane_off + s_col(sbuf), sr);
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) tmem_ld32(tmem + lane_off + s_col(sbuf) + c * 32, sr + c * 32);
         tmem_wait_ld();
         const int k0 = lo + j * BK;
         const int n_valid = min(BK, hi - k0);
         float s[BK];
 #pragma unroll
         for (int c = 0; c < BK; ++c) s[c] = (c < n_valid) ? __uint_as_float(sr[c]) : -INFINITY;
-        float mx = s[0];
+        // row maximum: 8 chains of three-input max, then a tree
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < BK; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c + 16 <= BK; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+        if ((BK - 8) % 16 == 8) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BK - 8 + i]);
+        }
+        float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
         mx *= a.scale_log2;
         const bool need = mx > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -441,7 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[c] = pack_bf16x2(p0, p1);
         }
         l_run += rs;
-        tmem_st16(tmem + lane_off + s_col(sbuf), pr);
+        if constexpr (BK == 32)
+          tmem_st16(tmem + lane_off + s_col(sbuf), pr);
+        else
+          tmem_st32(tmem + lane_off + s_col(sbuf), pr);
         if (n_valid < BK) {
           // rows past the sequence may hold anything: clear their value dims so that P V stays finite
           uint8_t* tile_smem = smem + kKOff + st * kTileBytes;

@@ -12,10 +12,15 @@
 //   warps 0, 2  TMA producers: K tiles (warp 0), and the Q tiles of each work
 //               item followed by its V tiles (warp 2), through rings of
 //               shared-memory stages (128-byte swizzle).
-//   warps 1, 3  MMA issuers, one lane per Q tile: S_t = Q_t K_j^T (A, B from
-//               shared memory) and O_t += P_t V_j (P read from TMEM, V from
-//               shared memory as an MN-major operand).  Warp 1 also allocates
-//               the 512 TMEM columns.
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//               S_t = Q_t K_j^T (A, B from shared memory) and O_t += P_t V_j
+//               (P read from TMEM, V from shared memory as an MN-major operand).
+//               A tcgen05.mma is accepted only as the tensor pipe frees a slot,
+//               so the lane does every wait of a tile first and then issues its
+//               P V and Q K as one burst.  (One issuing lane per Q tile was
+//               measured 15% slower: the two tiles' MMAs then interleave and
+//               each tile's chain through its softmax gets longer.)
+//   warp 3      idle (gives its registers to the softmax warpgroups)
 //   warps 4-7   softmax warpgroup of Q tile 0, warps 8-11 of Q tile 1: each thread
 //               owns one query row (TMEM lane), so row max / row sum need no
 //               shuffles.  P is written back over S in TMEM as bf16.  The output
@@ -239,13 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 2);  // released by both MMA issuers
+      mbar_init(&bars->k_empty[s], 1);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 2);
+      mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->fin, 2);
+    mbar_init(&bars->fin, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -269,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto q_smem = [&](int t) { return smem + C::kQOff + t * C::kQKTileBytes; };
 
   if (warp < 4) {
-    // control warpgroup: TMA producers (warps 0, 2) and the MMA issuers
-    // (warps 1, 3); its registers go to the softmax warpgroups
+    // control warpgroup: TMA producers (warps 0, 2), the MMA issuer (warp 1)
+    // and an idle warp; its registers go to the softmax warpgroups
     setmaxnreg_dec<kRegsCtl>();
     if (warp == 0 || warp == 2) {
       // ------------------------------------------------------------ TMA producers
@@ -322,96 +327,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-    } else {
-      // ------------------------------------------------------------ MMA issuers
-      // One issuing lane per Q tile (warp 1: tile 0, warp 3: tile 1), so that
-      // the waits and bookkeeping of one tile overlap the other tile's MMAs
-      // (a tcgen05.mma is accepted only as the tensor pipe frees a slot, so a
-      // single issuer serialises every wait with the pipe).  Per member key tile
-      // m_i of its range: P V(m_{i-1}) then Q K(m_i), back to back (QK reuses
-      // the S/P columns the P V reads, so the two stay ordered in one thread).
-      // Both issuers walk every loaded tile of both rings, releasing each stage
-      // once (empty barriers count two arrivals), after its full barrier; a
-      // pending P V is issued before passing a tile the Q tile does not need, so
-      // no issuer holds a V stage while it waits for a later one.
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      // One lane issues both tiles' MMAs.  Per loaded key tile j: for each Q tile
+      // t that needs it, every wait first (P_t(j) ready, K(j+1) landed), then
+      // P_t V(j) and Q_t K(j+1) back to back, so the tensor pipe sees one burst.
       if (lane == 0) {
-        const int t = warp == 1 ? 0 : 1;
-        const uint64_t q_desc = sdesc_sw128(smem_u32(q_smem(t)), 16, 1024);
+        const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem(0)), 16, 1024);
         const uint64_t k_desc0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
         const uint64_t v_desc0 = sdesc_sw128(smem_u32(smem + C::kVOff), C::kBlockBytes, 1024);
-        const uint32_t s_tm = tmem + t * 128u, o_tm = tmem + C::kOCol0 + t * DV;
-        uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph = 0;
+        uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph0 = 0, pph1 = 0;
         uint32_t it = 0;
-        // Descriptors advance by adding offsets in 16-byte units to the start-
-        // address field (shared-memory addresses stay below 256 KB, so the 14-bit
-        // field never carries); the K loops are unrolled.
-        auto issue_qk = [&](uint32_t stage) {
+        auto issue_qk = [&](int t, uint32_t stage) {
+          const uint64_t a0 = q_desc0 + ((t * C::kQKTileBytes) >> 4);
           const uint64_t b0 = k_desc0 + ((stage * C::kQKTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBlockBytes + (kk & 3) * 32) >> 4;
-            mma_ss(s_tm, q_desc + off, b0 + off, C::kIdescQK, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + t * 128u, a0 + off, b0 + off, C::kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_pv = [&](uint32_t stage, bool accumulate) {
+        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
           const uint64_t b0 = v_desc0 + ((stage * C::kVTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(o_tm, s_tm + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-        };
-        // P V of the pending member tile (its V ring entry is prev_vst / prev_vph)
-        bool have_prev = false, pv_started = false;
-        uint32_t prev_vst = 0, prev_vph = 0;
-        auto issue_pending_pv = [&]() -> bool {
-          if (!mbar_wait(&bars->p_full[t], pph, wc)) return false;
-          pph ^= 1;
-          if (!pv_started && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) return false;
-          if (!mbar_wait(&bars->v_full[prev_vst], prev_vph, wc)) return false;
-          tc_fence_after();
-          issue_pv(prev_vst, pv_started);
-          pv_started = true;
-          mma_commit(&bars->v_empty[prev_vst]);
-          have_prev = false;
-          return true;
+            mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
+                   (accumulate || kk > 0) ? 1u : 0u);
         };
         for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
           const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
-          const TileRange rng = t ? itm.r1 : itm.r0;
-          bool q_seen = false;
-          pv_started = false;
-          for (int v = 0; v < itm.n_load; ++v) {
-            const bool mine = rng.has(itm.load_at(v));
-            if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
-            if (mine) {
-              // P V of the previous member and Q K of this one, back to back
-              if (have_prev && !issue_pending_pv()) goto mma_done;
-              if (!q_seen) {
-                if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
-                q_seen = true;
-                tc_fence_after();
-              }
-              issue_qk(kst);
+          bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
+          if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
+          {
+            const int j0 = itm.load_at(0);
+            for (int t = 0; t < 2; ++t) {
+              if (!(t ? itm.r1 : itm.r0).has(j0)) continue;
+              if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+              (t ? q_seen1 : q_seen0) = true;
+              tc_fence_after();
+              issue_qk(t, kst);
               mma_commit(&bars->s_full[t]);
-              mma_commit(&bars->k_empty[kst]);
-              have_prev = true;
-              prev_vst = vst;
-              prev_vph = vph;
-            } else {
-              // a tile only the other Q tile needs: finish the pending P V (so no
-              // V stage stays held), then pass both ring entries on
-              if (have_prev && !issue_pending_pv()) goto mma_done;
-              mbar_arrive(&bars->k_empty[kst]);
-              if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
-              mbar_arrive(&bars->v_empty[vst]);
             }
-            if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
-            if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
           }
-          if (have_prev && !issue_pending_pv()) goto mma_done;  // the last member tile
-          mma_commit(&bars->o_done[t]);
+          mma_commit(&bars->k_empty[kst]);
+          if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+          for (int v = 0; v < itm.n_load; ++v) {
+            const int j = itm.load_at(v);
+            const bool next = v + 1 < itm.n_load;
+            const int jn = next ? itm.load_at(v + 1) : -1;
+            if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+            bool k_ready = false;
+            for (int t = 0; t < 2; ++t) {
+              const TileRange& r = t ? itm.r1 : itm.r0;
+              const bool pv = r.has(j), qk = next && r.has(jn);
+              if (pv) {
+                if (!mbar_wait(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
+                if (t) pph1 ^= 1; else pph0 ^= 1;
+                if (!(t ? pv_seen1 : pv_seen0) && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
+              }
+              if (qk) {
+                if (!k_ready) {
+                  if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
+                  k_ready = true;
+                }
+                if (!(t ? q_seen1 : q_seen0) && !mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+                if (t) q_seen1 = true; else q_seen0 = true;
+              }
+              tc_fence_after();
+              if (pv) {
+                issue_pv(t, vst, t ? pv_seen1 : pv_seen0);
+                if (t) pv_seen1 = true; else pv_seen0 = true;
+                if (j == r.jh) mma_commit(&bars->o_done[t]);
+              }
+              if (t == 1) {
+                mma_commit(&bars->v_empty[vst]);
+                if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
+              }
+              if (qk) {
+                issue_qk(t, kst);
+                mma_commit(&bars->s_full[t]);
+              }
+            }
+            if (next) {
+              mma_commit(&bars->k_empty[kst]);
+              if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+            }
+          }
         }
       mma_done:
-        // every MMA this lane issued completes before TMEM is released
+        // every MMA issued so far completes before TMEM is released
         mma_commit(&bars->fin);
         drain_wait(&bars->fin, 0, a.wait_limit_ns);
       }
