@@ -10,13 +10,17 @@
 // Mapping.  The fp32 output O is 128 heads x 512 dims = all 512 TMEM columns of
 // an SM, leaving no room for the scores, so CTAs work in pairs: both CTAs of a
 // pair walk the same keys, each computes the full score tile S = Q C^T (M = 128
-// heads, N = 32 keys, K = 576) and its own softmax, and each accumulates half of
-// the value dims (O_half += P V_half, M = 128, N = 256, K = 32).  The pair
-// reads every cache row from L2 twice but from HBM once.  The query is the
-// MMA's A operand: its first 384 dims sit in the TMEM columns left free by S and
-// O_half (bf16 pairs, written by the softmax warps), the last 192 dims in shared
-// memory (48 KB), which leaves room for a 4-stage ring of 32-key cache tiles
-// (36 KB each), loaded by TMA with 128-byte swizzle.
+// heads, N = 64 keys, K = 576) and its own softmax, and each accumulates half of
+// the value dims (O_half += P V_half, M = 128, N = 256, K = 64).  The pair
+// reads every cache row from L2 twice but from HBM once.  A tcgen05.mma costs
+// the same time at N = 64 as at N = 128 (and at N = 32), so the key tile is as
+// wide as TMEM allows: two 64-column S/P buffers, O_half (256 columns) and the
+// query's first 256 dims (128 columns of bf16 pairs, the MMA's A operand,
+// written by the softmax warps) fill the 512 columns; the query's other 320
+// dims sit in shared memory (80 KB) beside a 2-stage ring of 64-key cache tiles
+// (72 KB each), loaded by TMA with 128-byte swizzle.  (32-key tiles with a
+// 4-stage ring ran 1.55x slower.)  The batch's key prefix sums live in shared
+// memory too, which caps this kernel at 256 sequences per call.
 // Keys of all sequences, laid end to end, are split evenly over the pairs
 // (a pair's range may cross sequence boundaries), so every pair does the same
 // work; each (pair, sequence) piece writes one normalised partial, merged per
@@ -63,7 +67,7 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(NH, BK, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(NH, DVH, true);
 constexpr float kRescaleThreshold = 8.0f;
 #ifndef ATTN_MLA_PREFETCH_TILES
-#define ATTN_MLA_PREFETCH_TILES 8
+#define ATTN_MLA_PREFETCH_TILES 4
 #endif
 constexpr int kPrefetchTiles = ATTN_MLA_PREFETCH_TILES;  // tiles requested into L2 ahead of the smem loads
 
