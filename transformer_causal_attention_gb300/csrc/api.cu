@@ -441,7 +441,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   const bool chunked_rope = !rope || (rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0);
   const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, bf16) &&
                        decode_mla_supported(B, n_h, n_kv, D_qk, D_v, ldv, vcache == kcache, bf16) &&
-                       chunked_rope && (!rope || rope_offset >= kMlaQTmemDims);
+                       chunked_rope && (!rope || decode_mla_rope_ok(rope_offset, rope_dims, half));
   if (use_mla) {
     ns = decode_mla_pairs(dev.sms);  // the kernel runs 2 CTAs per pair
     chunk = 0;

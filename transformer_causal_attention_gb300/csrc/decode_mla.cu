@@ -608,6 +608,11 @@ bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long
          B <= kMaxB;
 }
 
+bool decode_mla_rope_ok(int rope_offset, int rope_dims, bool half) {
+  // the rotated span lies in the shared-memory part of the query, in whole 8-dim chunks
+  return rope_offset >= kQTmemDims && rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0;
+}
+
 int decode_mla_pairs(int num_sms) {
   const int p = num_sms / 2;
   return p < 1 ? 1 : (p > kMlaMaxPairs ? kMlaMaxPairs : p);

@@ -102,10 +102,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const RopeFreq& rope, bool bf16, 
 cudaError_t launch_decode_combine(const DecodeArgs& a, bool bf16, cudaStream_t st, int* launches);
 constexpr int kMlaMaxPairs = 128;  // CTA pairs of the MLA decode kernel (workspace is sized for this)
 constexpr int kMlaTileKeys = 64;   // keys per cache tile (TMA box rows) of the MLA decode kernel
-constexpr int kMlaQTmemDims = 256; // query dims [0, kMlaQTmemDims) held in TMEM; RoPE must lie above them
+constexpr int kMlaQTmemDims = 256; // query dims [0, kMlaQTmemDims) held in TMEM
 bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long v_token_stride, bool v_is_k,
                           bool bf16);
 int decode_mla_pairs(int num_sms);
+// Whether the MLA kernel can rotate the query span [rope_offset, rope_offset + rope_dims).
+bool decode_mla_rope_ok(int rope_offset, int rope_dims, bool half);
 cudaError_t launch_decode_mla(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, cudaStream_t st,
                               int* launches);
 constexpr int kStreamTileKeys = 64;  // keys per TMA box of the streaming GQA decode
