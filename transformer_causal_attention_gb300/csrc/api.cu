@@ -461,6 +461,16 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
         !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, kMlaTileKeys))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);
+  } else if (window == 0 && decode_tc_supported(n_h, n_kv, D_qk, D_v, bf16, rope_offset, rope_dims, rope)) {
+    // K and V tiles of 128 keys on the tensor cores (keys on M, the head group on N)
+    CUtensorMap maps[2];
+    const unsigned long long ks = static_cast<unsigned long long>(D_qk) * 2;
+    const unsigned long long vs = static_cast<unsigned long long>(ldv) * 2;
+    if (!make_map4(&maps[0], kcache, D_qk, n_kv, max_len, B, ks, ks * n_kv, ks * n_kv * max_len, kStreamTileKeys) ||
+        !make_map4(&maps[1], vcache, D_v, n_kv, max_len, B, static_cast<unsigned long long>(D_v) * 2, vs,
+                   vs * max_len, kStreamTileKeys))
+      return finish(cudaErrorInvalidValue, launches);
+    e = launch_decode_tc(da, rf, maps, dev.sms, st, &launches);
   } else if (window == 0 && chunked_rope && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
     // K and V stream through shared memory in 64-key tiles
     CUtensorMap maps[2];
