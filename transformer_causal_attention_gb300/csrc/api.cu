@@ -470,7 +470,12 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
         !make_map4(&maps[1], vcache, D_v, n_kv, max_len, B, static_cast<unsigned long long>(D_v) * 2, vs,
                    vs * max_len, kStreamTileKeys))
       return finish(cudaErrorInvalidValue, launches);
-    e = launch_decode_tc(da, rf, maps, dev.sms, st, &launches);
+    // fewer, longer chunks than the generic plan: each chunk pays a query load, a
+    // pipeline fill and an epilogue (never more splits than the workspace holds)
+    DecodeArgs dt = da;
+    while (dt.chunk < kDecodeTcMinChunk && dt.chunk < max_len) dt.chunk *= 2;
+    dt.n_split = (max_len + dt.chunk - 1) / dt.chunk;
+    e = launch_decode_tc(dt, rf, maps, dev.sms, st, &launches);
   } else if (window == 0 && chunked_rope && decode_stream_supported(n_h, n_kv, D_qk, D_v, bf16)) {
     // K and V stream through shared memory in 64-key tiles
     CUtensorMap maps[2];
