@@ -367,7 +367,7 @@ size_t attn_decode_workspace_size(int B, int n_h, int n_kv, int D_qk, int D_v, i
     if (mla_slots > slots) slots = mla_slots;
   }
   const size_t o_bytes = (slots * D_v * sizeof(float) + 255) & ~size_t(255);
-  return o_bytes + ((slots * sizeof(float) + 255) & ~size_t(255));
+  return o_bytes + ((slots * sizeof(float) + 255) & ~size_t(255)) + 256;  // + scheduler counters
 }
 
 namespace attn {
@@ -437,6 +437,8 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            ((slots * D_v * sizeof(float) + 255) & ~size_t(255)));
+  unsigned int* ws_ctr = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws_lse) +
+                                                         ((slots * sizeof(float) + 255) & ~size_t(255)));
   // the tensor-core and streaming kernels rotate whole 8-dim chunks of the query
   const bool chunked_rope = !rope || (rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0);
   const bool use_mla = window == 0 && mla_shape(B, n_h, n_kv, D_qk, D_v, bf16) &&
@@ -449,7 +451,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D_qk));
   DecodeArgs da{q, kcache, vcache, ldv, seqlens, out, lse, B, n_h, n_kv, D_qk, D_v, max_len,
                 rope ? rope_offset : 0, sc * kLog2e, ws_o, ws_lse, ns, chunk, dev.status, g_wait_limit_ns.load(),
-                window, n_sink};
+                window, n_sink, ws_ctr};
   int launches = 0;
   const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0, half);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

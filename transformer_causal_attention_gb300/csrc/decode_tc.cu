@@ -22,11 +22,14 @@
 //
 // Roles (256 threads, one persistent CTA per SM): warp 0 TMA producer (K and
 // V tiles of 128 keys, two 64-row boxes per 64-dim block, through a 3-stage
-// ring of 64 KB; the whole unit is first requested into L2), warp 1 TMEM
-// owner and single-thread MMA issuer, warps 4-7 softmax and epilogue.  Work
-// units are (sequence, chunk of keys, KV head) with the KV head fastest, as in
-// the CUDA-core streaming kernel; each writes one normalised partial per head,
-// merged by the combine kernel of decode.cu.
+// ring of 64 KB; L2 prefetches ahead of the loads measured slower at this
+// rate), warp 1 TMEM owner and single-thread MMA issuer, warps 4-7 softmax and
+// epilogue.  Work units are (sequence, chunk of keys, KV head) with the KV head
+// fastest, as in the CUDA-core streaming kernel; the producer claims them from
+// a global counter (sequence lengths differ, so a static split left the
+// busiest SM 9% above the mean) and hands each to the consumers through a
+// small shared-memory queue.  Each unit writes one normalised partial per
+// head, merged by the combine kernel of decode.cu.
 #include <math.h>
 
 #include "kernels.h"
@@ -59,6 +62,7 @@ constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(BK, NHP, false);                  // A, B K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(D, NHP, false) | (1u << 15);     // A (V^T) MN-major
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kUnitSlots = 4;               // work units handed from the producer to the consumers
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
@@ -66,6 +70,8 @@ struct Bars {
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_empty, fin;
   uint64_t red;  // softmax-thread barrier (128 arrivals per phase)
+  uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
+  int unit_q[kUnitSlots];  // claimed unit index, -1: no more work
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -157,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_empty, 128);
     mbar_init(&bars->fin, 1);
     mbar_init(&bars->red, 128);
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(&bars->unit_full[s], 1);
+      mbar_init(&bars->unit_empty[s], 1 + 128);  // the MMA issuer and every softmax thread
+    }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -179,15 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t st = 0, ph = 0, issued = 0, last_ph = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      uint32_t st = 0, ph = 0, issued = 0, last_ph = 0, qs = 0, qph = 0;
+      for (;;) {
         Unit w;
-        if (!unit_at(u, a, w)) continue;
-        for (int k0 = w.start; k0 < w.end; k0 += kBox)  // the whole unit on its way into L2
-          for (int db = 0; db < D / 64; ++db) {
-            tma_prefetch_l2_4d(&tm_k, db * 64, w.g, k0, w.b);
-            tma_prefetch_l2_4d(&tm_v, db * 64, w.g, k0, w.b);
-          }
+        int u;
+        do {  // claim the next non-empty unit
+          u = static_cast<int>(atomicAdd(a.ws_counter, 1u));
+        } while (u < n_units && !unit_at(u, a, w));
+        if (!mbar_wait(&bars->unit_empty[qs], qph ^ 1, wc)) goto producer_done;
+        bars->unit_q[qs] = u < n_units ? u : -1;
+        mbar_arrive(&bars->unit_full[qs]);
+        if (++qs == kUnitSlots) { qs = 0; qph ^= 1; }
+        if (u >= n_units) break;
         for (int k0 = w.start; k0 < w.end; k0 += BK) {
           if (!mbar_wait(&bars->empty[st], ph ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
@@ -217,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc0 = sdesc_sw128(smem_u32(smem + kKVOff + kTileBytes), kBlockBytes, 1024);
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + kQOff), 16, 1024);
       const uint64_t p_desc0 = sdesc_sw128(smem_u32(smem + kPOff), 16, 1024);
-      uint32_t st = 0, ph = 0, pph = 0, tile = 0, n = 0;
+      uint32_t st = 0, ph = 0, pph = 0, tile = 0, n = 0, qs = 0, qph = 0;
       // Descriptors advance by adding offsets in 16-byte units to the start-address
       // field (shared-memory addresses stay below 256 KB: the field never carries).
       auto issue_qk = [&](uint32_t stage, uint32_t sbuf) {
@@ -236,9 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                  b0 + (((kk >> 2) * kPBlockBytes + (kk & 3) * 32) >> 4), kIdescPV,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (;;) {
+        if (!mbar_wait(&bars->unit_full[qs], qph, wc)) goto mma_done;
+        const int u = bars->unit_q[qs];
+        mbar_arrive(&bars->unit_empty[qs]);
+        if (++qs == kUnitSlots) { qs = 0; qph ^= 1; }
+        if (u < 0) break;
         Unit w;
-        if (!unit_at(u, a, w)) continue;
+        unit_at(u, a, w);
         const int nt = (w.end - w.start + BK - 1) / BK;
         if (!mbar_wait(&bars->q_ready, n & 1, wc)) goto mma_done;
         if (!mbar_wait(&bars->full[st], ph, wc)) goto mma_done;
@@ -281,10 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp & 3;             // TMEM lane quadrant
     const int k = sw * 32 + lane;        // key row of a tile / value dim of O^T (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(sw * 32) << 16;
-    uint32_t sph = 0, pvph = 0, rph = 0, st = 0, tile = 0, n = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    uint32_t sph = 0, pvph = 0, rph = 0, st = 0, tile = 0, n = 0, qs = 0, qph = 0;
+    for (;;) {
+      if (!warp_wait(&bars->unit_full[qs], qph, wc)) break;
+      const int u = bars->unit_q[qs];
+      mbar_arrive(&bars->unit_empty[qs]);
+      if (++qs == kUnitSlots) { qs = 0; qph ^= 1; }
+      if (u < 0) break;
       Unit w;
-      if (!unit_at(u, a, w)) continue;
+      unit_at(u, a, w);
       const int nt = (w.end - w.start + BK - 1) / BK;
       const int h0 = w.g * G;
       // Q_g into shared memory (rows = heads, K-major, 128-byte swizzle), rotated at
@@ -465,6 +488,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const RopeFreq& rope, const CU
                              cudaStream_t st, int* launches) {
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(a.ws_counter, 0, sizeof(unsigned int), st)) != cudaSuccess) return e;  // unit claims
   const long long units = static_cast<long long>(a.B) * a.n_kv * a.n_split;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   decode_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(a, rope, maps[0], maps[1]);

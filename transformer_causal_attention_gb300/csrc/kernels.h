@@ -48,6 +48,7 @@ struct DecodeArgs {
   unsigned long long wait_limit_ns;
   int window;  // > 0: the new token (position L-1) sees keys n with L-1-n < window, plus n < n_sink
   int n_sink;
+  unsigned int* ws_counter;  // scratch counter in the workspace (work claims of the tensor-core GQA decode)
 };
 
 // Visible keys of a decode query at position L - 1: [0, L) without a window,
