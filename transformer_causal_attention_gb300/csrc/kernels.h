@@ -112,7 +112,7 @@ bool decode_mla_rope_ok(int rope_offset, int rope_dims, bool half);
 cudaError_t launch_decode_mla(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, cudaStream_t st,
                               int* launches);
 constexpr int kStreamTileKeys = 64;  // keys per TMA box of the streaming GQA decode
-constexpr int kDecodeTcMinChunk = 1024;  // keys per work unit of the tensor-core GQA decode, at least
+constexpr int kDecodeTcMinChunk = 4096;  // keys per work unit of the tensor-core GQA decode, at least
 bool decode_tc_supported(int n_h, int n_kv, int D_qk, int D_v, bool bf16, int rope_offset, int rope_dims, bool rope);
 cudaError_t launch_decode_tc(const DecodeArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
                              cudaStream_t st, int* launches);
