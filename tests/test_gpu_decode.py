@@ -170,3 +170,27 @@ def test_decode_sliding_window_with_sinks(lib, name, window, sink):
                                            scale=cfg["scale"], window=window, n_sink=sink)
     assert_parity(out, ref, "bf16", f"{name} window {window}")
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+TC_GQA = [
+    # B, n_h, n_kv, max_len, rope_base: head groups of 1..16 on the tensor-core GQA kernel
+    (3, 8, 8, 333, 1e4),      # G = 1 (MHA): one real row of the N = 16 operand
+    (2, 16, 8, 129, 0.0),     # G = 2, one key past a tile
+    (2, 32, 4, 1000, 5e5),    # G = 8
+    (2, 64, 4, 260, 1e4),     # G = 16: the whole padded operand
+    (2, 32, 8, 9000, 5e5),    # several 4096-key work units per sequence
+    (5, 32, 8, 128, 5e5),     # exactly one tile
+]
+
+
+@pytest.mark.parametrize("B,n_h,n_kv,L,rope", TC_GQA)
+def test_tensor_core_gqa_decode_head_groups(lib, B, n_h, n_kv, L, rope):
+    cfg = dict(B=B, n_h=n_h, n_kv=n_kv, D_qk=128, D_v=128, max_len=L, len_lo=1, len_hi=L, v_aliases_k=False,
+               dtype="bf16", rope_base=rope, rope_offset=0, rope_dims=128, scale=0.0)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=L + n_h)
+    sl[0] = 1
+    sl[-1] = L
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", f"tensor-core GQA decode {cfg}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
