@@ -297,8 +297,9 @@ ATTN_API int attn_decode_static(const void* q, const void* kcache, const void* v
 /*
  * attn_device_status - synchronise the stream, then return ATTN_OK, or
  * ATTN_ERR_TIMEOUT if a kernel of this library gave up on a bounded wait since
- * the last call (the flag is cleared), or ATTN_ERR_CUDA if the stream reports
- * an error.
+ * the last call, or ATTN_ERR_CUDA if the stream reports an error or a kernel
+ * found its shared memory laid out other than it requires (and skipped its
+ * work); the device flags are cleared.
  */
 ATTN_API int attn_device_status(void* stream);
 

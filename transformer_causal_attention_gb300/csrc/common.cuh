@@ -13,7 +13,7 @@
 namespace attn {
 
 // Status bits a kernel ORs into the caller-visible status word.
-enum : unsigned int { STATUS_TIMEOUT = 1u };
+enum : unsigned int { STATUS_TIMEOUT = 1u, STATUS_LAYOUT = 2u };  // LAYOUT: shared memory not as required
 
 // Frequencies of the RoPE pairs, in turns per position: f_i = theta_i / (2*pi)
 // with theta_i = base^(-2i / D_r).  Each f_i is split into hi + lo floats by the

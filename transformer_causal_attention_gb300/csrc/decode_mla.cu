@@ -41,7 +41,7 @@ constexpr int DQK = 576;         // latent + rotary dims
 constexpr int DV = 512;          // value dims
 constexpr int DVH = 256;         // value dims per CTA of a pair
 constexpr int BK = kMlaTileKeys;  // keys per tile (MMA N of the score tile)
-constexpr int kStages = BK == 32 ? 4 : 2;
+constexpr int kStages = BK == 32 ? 4 : (BK == 48 ? 3 : 2);
 constexpr int kThreads = 256;
 constexpr int kBlocks = DQK / 64;                  // 9 column blocks of 64 dims
 constexpr int kQTmemDims = kMlaQTmemDims;          // query dims [0, kQTmemDims) live in TMEM (A operand)
@@ -50,12 +50,15 @@ constexpr int kQBlockBytes = NH * 128;             // 16 KB
 constexpr int kQSmemBytes = kQSmemBlocks * kQBlockBytes;  // 48 KB
 constexpr int kKBlockBytes = BK * 128;             // 4 KB
 constexpr int kTileBytes = kBlocks * kKBlockBytes; // 36 KB
-constexpr int kMaxB = BK == 32 ? 1024 : 256;  // the key prefix sums of the batch live in shared memory
+constexpr int kMaxB = BK == 32 ? 1024 : (BK == 48 ? 128 : 256);  // the batch's key prefix sums live in smem
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQSmemBytes;
 constexpr int kPrefOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kPrefOff + (kMaxB + 1) * 4 + 60;
-constexpr int kSmemBytes = kBarOff + 160 + 1024;
+constexpr int kUsedBytes = kBarOff + 160;
+// The dynamic shared memory is declared 1024-byte aligned; the slack for aligning it
+// by hand is kept wherever it fits (the kernel checks the alignment at run time).
+constexpr int kSmemBytes = kUsedBytes + 1024 <= 227 * 1024 ? kUsedBytes + 1024 : kUsedBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 // TMEM columns: S/P buffer b at [BK b, BK b + BK), O_half at [2 BK, 2 BK + 256), then the query dims
 // [0, kQTmemDims) as bf16 pairs
@@ -138,6 +141,19 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
   }
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -150,8 +166,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (static_cast<int>(smem - smem_raw) + kUsedBytes > kSmemBytes) {  // not enough slack: report, touch nothing
+    if (threadIdx.x == 0) atomicOr(a.status, STATUS_LAYOUT);
+    return;
+  }
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   int* prefix = reinterpret_cast<int*>(smem + kPrefOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -422,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[BK];
 #pragma unroll
         for (int c = 0; c < BK / 32; ++c) tmem_ld32(tmem + lane_off + s_col(sbuf) + c * 32, sr + c * 32);
+        if constexpr (BK % 32 == 16) tmem_ld16(tmem + lane_off + s_col(sbuf) + BK - 16, sr + BK - 16);
         tmem_wait_ld();
         const int k0 = lo + j * BK;
         const int n_valid = min(BK, hi - k0);
@@ -459,10 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[c] = pack_bf16x2(p0, p1);
         }
         l_run += rs;
-        if constexpr (BK == 32)
-          tmem_st16(tmem + lane_off + s_col(sbuf), pr);
-        else
-          tmem_st32(tmem + lane_off + s_col(sbuf), pr);
+        // P as bf16 pairs: BK / 2 columns
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) tmem_st32(tmem + lane_off + s_col(sbuf) + c * 32, pr + c * 32);
+        if constexpr ((BK / 2) % 32 == 16) tmem_st16(tmem + lane_off + s_col(sbuf) + BK / 2 - 16, pr + BK / 2 - 16);
+        if constexpr ((BK / 2) % 32 == 24) {
+          tmem_st16(tmem + lane_off + s_col(sbuf) + (BK / 64) * 32, pr + (BK / 64) * 32);
+          tmem_st8(tmem + lane_off + s_col(sbuf) + (BK / 64) * 32 + 16, pr + (BK / 64) * 32 + 16);
+        }
         if (n_valid < BK) {
           // rows past the sequence may hold anything: clear their value dims so that P V stays finite
           uint8_t* tile_smem = smem + kKOff + st * kTileBytes;
