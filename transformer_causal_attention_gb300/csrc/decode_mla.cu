@@ -27,11 +27,17 @@
 // side brings the two halves to the larger offset by scaling O or the peer's P
 // down - both factors are at most one.
 //
+// The copy goes out as asynchronous remote stores that count their bytes on the
+// peer's barrier (st.async with complete_tx), so no fence or remote arrive is
+// on the sending side.
+//
 // Loads.  Cache rows stream through a 3-stage ring of 32 KB units (128 keys x
 // 128 dims, two 128-byte-swizzled TMA boxes): five units per round for the
 // scores (the 576 dims), then two of the own keys and two of the peer's keys
 // for P V, restricted to this CTA's value dims (the second read of a row hits
-// L2).  The query's dims [0, 256) live in TMEM (the score MMA's A operand),
+// L2).  No L2 prefetch: requests ahead of the ring (tensor or bulk prefetch
+// through the TMA engine, or plain prefetches from an idle warp) measured
+// slower or equal.  The query's dims [0, 256) live in TMEM (the score MMA's A operand),
 // dims [256, 576) in shared memory.  Rows at or past a sequence's end may hold
 // anything, so a helper warp zeroes them in the value units before their MMA.
 //
@@ -88,7 +94,8 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(NH, RK, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(NH, 128, true);
 constexpr float kRaise = 8.0f;       // the shared offset moves when a row maximum passes it by 2^8
 constexpr float kEmergency = 64.0f;  // a CTA uses its own maximum when its scores pass the offset by 2^64
-constexpr int kPrefetchRounds = 2;   // own-key rounds requested into L2 ahead of the loads
+// bytes the peer stores per round: P (128 heads x 128 keys bf16), offsets, maxima, row sums
+constexpr uint32_t kMsgBytes = NH * RK * 2 + 4 * NH * 4;
 
 struct Msg {  // written by the peer CTA each round
   float m_own[NH];  // offset its P used
@@ -205,18 +212,19 @@ __device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
+// Asynchronous stores into the peer CTA's shared memory; each counts its bytes on the
+// peer's barrier (complete_tx), so the peer sees them once its barrier phase completes.
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                           uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -303,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->pvo_done, 1);
-    mbar_init(&bars->pp_full, 256);
+    mbar_init(&bars->pp_full, 1);  // armed locally each round with the message's byte count
+    mbar_arrive_expect_tx(&bars->pp_full, kMsgBytes);  // round 0, before the peer can store
     mbar_init(&bars->pp_ready, 256);
     mbar_init(&bars->pvp_done, 1);
     mbar_init(&bars->pp_empty, 1);
@@ -364,18 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int blk = 0; blk < kQSmemBlocks; ++blk)
           tma_load_3d(smem + kQOff + blk * kBlockBytes, &tm_q, &bars->q_full, kQTmemDims + blk * 64, 0, sb);
         q_issued = n + 1;
-        auto prefetch_round = [&](int j) {
-          const int k0 = lo + j * kRoundKeys + r * RK;
-          if (j < nr && k0 < hi)
-            for (int blk = 0; blk < DQK / 64; ++blk) tma_prefetch_l2_3d(&tm_c, blk * 64, k0, sb);
-        };
-        for (int j = 0; j < kPrefetchRounds; ++j) prefetch_round(j);
-        int last_j = 0;
-        const bool done = for_units(lo, nr, r, [&](const Unit& u, int j) -> bool {
-          if (j != last_j) {  // first unit of a later round's scores: keep the L2 requests ahead
-            last_j = j;
-            if (!u.pv) prefetch_round(j + kPrefetchRounds - 1);
-          }
+        const bool done = for_units(lo, nr, r, [&](const Unit& u, int) -> bool {
           if (!mbar_wait(&bars->kv_empty[st], ph ^ 1, wc)) return false;
           const bool fix = needs_fix(u, L);
           uint64_t* bar = fix ? &bars->kv_tofix[st] : &bars->kv_full[st];
@@ -555,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     PieceIter it;
     it.init(prefix, a.B, k_begin, k_end);
     uint32_t G = 0, pvo_w = 0, pvp_w = 0, hs = 0;  // hs: uses of hsync[quad]
+    const bool armer = warp == 4 && lane == 0;  // arms pp_full for each later round's message
     int sb, lo, hi;
     for (uint32_t n = 0; run && it.next(&sb, &lo, &hi); ++n) {
       const int L = prefix[sb + 1] - prefix[sb];
@@ -699,18 +698,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait_cluster(&bars->pp_empty, (G & 1) ^ 1, wc)) { ok = false; break; }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          st_peer_v4(pp_peer + ((i ^ (h & 7)) << 4), pr[4 * i], pr[4 * i + 1], pr[4 * i + 2], pr[4 * i + 3]);
+          st_peer_v4(pp_peer + ((i ^ (h & 7)) << 4), pr[4 * i], pr[4 * i + 1], pr[4 * i + 2], pr[4 * i + 3],
+                     ppfull_peer);
         if (kh == 0) {
-          st_peer_f32(msg_peer + h * 4, m_own);
-          st_peer_f32(msg_peer + (NH + h) * 4, mx_cta);
+          st_peer_f32(msg_peer + h * 4, m_own, ppfull_peer);
+          st_peer_f32(msg_peer + (NH + h) * 4, mx_cta, ppfull_peer);
         }
-        st_peer_f32(msg_peer + ((2 + kh) * NH + h) * 4, rs);
-        fence_proxy_async_cluster();
-        arrive_peer(ppfull_peer);
+        st_peer_f32(msg_peer + ((2 + kh) * NH + h) * 4, rs, ppfull_peer);
 
         // the peer's round: bring O, l and the peer's P to one offset
         if (!warp_wait_cluster(&bars->pp_full, G & 1, wc)) { ok = false; break; }
         const float m_p = msg->m_own[h], mx_p = msg->mx[h], rs_p = msg->rs[kh][h];
+        // the next message may land only after this CTA's P V(peer) of this round has completed,
+        // which follows every thread's pp_ready below: arming the next phase here precedes it
+        if (armer) mbar_arrive_expect_tx(&bars->pp_full, kMsgBytes);
         if (!warp_wait(&bars->pvo_done, pvo_w & 1, wc)) { ok = false; break; }
         ++pvo_w;
         if (pvp_w < G) {
