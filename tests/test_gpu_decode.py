@@ -124,6 +124,31 @@ def test_mla_shaped_decode(lib, B, L, rope):
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
 
 
+def test_mla_decode_score_spikes(lib):
+    """A few cached keys score about 80 (natural log units) above everything else for one head
+    each, at positions spread over the sequences, so that most of them arrive after a CTA pair has
+    fixed its shared exponent offset: the tensor-core MLA kernel must then move a row's offset
+    within a round (its scores pass the old offset by far more than bf16 / fp32 exponents allow)
+    and bring the two halves of the pair back to one offset.  Random inputs never take that path."""
+    cfg = workloads.config("mla_decode", B=4, max_len=32768, len_lo=32768, len_hi=32768, rope_base=0.0)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=5)
+    scale = 1.0 / math.sqrt(192.0)
+    spikes = [(0, 700, 3), (0, 5000, 77), (0, 17000, 127), (0, 30001, 40), (2, 1500, 0), (2, 20000, 64),
+              (3, 32767, 100)]  # (sequence, key, head)
+    for b, t, h in spikes:
+        qh = q[b, h].double()
+        lam = 80.0 / (scale * float(qh @ qh))
+        kc[b, t, 0] = (lam * qh).to(kc.dtype)
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    idx = sorted({b for b, _, _ in spikes})
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl, batch_index=idx)
+    got = to_np(out)
+    assert_parity(got[idx], ref[idx], "bf16", "mla decode with score spikes")
+    assert np.max(np.abs(to_np(lse)[idx] - ref_lse[idx])) <= BF16_MAX_ABS
+    for b, t, h in spikes:  # the spiking key takes all of the head's weight
+        np.testing.assert_allclose(got[b, h], to_np(kc[b, t, 0, :512]), atol=BF16_MAX_ABS)
+
+
 @pytest.mark.parametrize("name", ["gqa_decode", "mla_decode"])
 def test_rows_past_seqlens_are_never_used(lib, name):
     # cache rows at or after seqlens[b] hold NaN: results must still match the oracle
