@@ -124,6 +124,20 @@ def test_mla_shaped_decode(lib, B, L, rope):
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
 
 
+@pytest.mark.parametrize("B", [256, 257])
+def test_mla_decode_batch_limit(lib, B):
+    # 256 sequences is the most the tensor-core MLA kernel takes (their key prefix sums live in
+    # shared memory), with many short sequences per CTA pair; one more runs on the generic kernel
+    cfg = workloads.config("mla_decode", B=B, max_len=64, len_lo=1, len_hi=64, rope_base=0.0)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=B)
+    sl[0] = 1
+    sl[-1] = 64
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", f"mla decode B={B}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
 def test_mla_decode_score_spikes(lib):
     """A few cached keys score about 80 (natural log units) above everything else for one head
     each, at positions spread over the sequences, so that most of them arrive after a CTA pair has
