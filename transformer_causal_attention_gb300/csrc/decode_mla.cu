@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       PieceIter it;
       it.init(prefix, a.B, k_begin, k_end);
       uint32_t st = 0, ph = 0, q_issued = 0, issued = 0;
-      uint64_t* last_bar[kStages] = {nullptr, nullptr, nullptr};
-      uint32_t last_par[kStages] = {0, 0, 0};
+      uint64_t* last_bar[kStages] = {};
+      uint32_t last_par[kStages] = {};
       uint32_t fullph = 0, fixph = 0;  // bit s: phase of kv_full[s] / kv_tofix[s]
       int sb, lo, hi;
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
