@@ -28,7 +28,8 @@
 //               (exact: l and O always share the same reference maximum).
 //   A work item is two adjacent Q tiles of one (batch, head); while one
 //   warpgroup computes its softmax, the tensor core runs the other tile's MMAs.
-//   Items are taken heaviest-first (latest Q tiles see the most keys).
+//   Items are taken heaviest-first (latest Q tiles see the most keys), dealt to the
+//   CTAs in waves that alternate direction.
 // RoPE: the query tile is rotated in shared memory right after its TMA load
 // (once per item); keys arrive already rotated (written once by the rope pass).
 // Head dims: (64, 64), (128, 128) and the MLA prefill shape D_qk = 192 (128
@@ -131,6 +132,15 @@ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, in
     r.ns = 0;
   }
   return r;
+}
+
+// Index of this CTA's k-th work item.  Items are sorted heaviest-first and dealt out in waves
+// of gridDim.x, every other wave in reverse CTA order, so that no CTA takes the heaviest item of
+// every wave (with one direction only, the busiest CTA of the Llama-3-8B prefill would carry
+// 3.5% more key tiles than the mean; alternating brings that to 0.1%).
+__device__ __forceinline__ int item_at(uint32_t k) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return static_cast<int>(k) * g + ((k & 1u) ? g - 1 - c : c);
 }
 
 __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n_pairs_q, int n_kt) {
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t st = 0, ph = 0;
         uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
         uint32_t q_issued = 0, it = 0;
-        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
+        for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
           const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
           if (is_v) {
             for (int t = 0; t < 2; ++t) {
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
+        for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
           const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
           if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
@@ -432,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + C::kOCol0 + (t ? DV : 0);
     uint32_t sph = 0;
     uint32_t it = 0;
-    for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it) {
+    for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
       const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
       const TileRange rng = t ? itm.r1 : itm.r0;
