@@ -37,9 +37,12 @@
 // for P V, restricted to this CTA's value dims (the second read of a row hits
 // L2).  No L2 prefetch: requests ahead of the ring (tensor or bulk prefetch
 // through the TMA engine, or plain prefetches from an idle warp) measured
-// slower or equal.  The query's dims [0, 256) live in TMEM (the score MMA's A operand),
-// dims [256, 576) in shared memory.  Rows at or past a sequence's end may hold
-// anything, so a helper warp zeroes them in the value units before their MMA.
+// slower or equal.  The query's dims [0, 256) live in TMEM (the score MMA's A
+// operand), dims [256, 576) in shared memory.  Rows at or past a sequence's end
+// may hold anything, so a helper warp zeroes them in the value units before
+// their MMA.  The tensor-core work of round j is issued as P V(own, j), the
+// scores of round j + 1, P V(peer, j): the peer's probabilities arrive while the
+// next scores run.
 //
 // Keys of all sequences, laid end to end, are split evenly over the pairs (a
 // pair's range may cross sequence boundaries), so every pair does the same
