@@ -197,6 +197,12 @@ def cpu_baseline_decode(q, kc, vc, sl, cfg, n_seq: int):
 
 
 # ------------------------------------------------------------------ reference arm
+# The workload both arms report (the reference arm times the oracle on samples of its prefill).
+WORKLOAD = ("llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
+            " + GQA decode 59 seqs L~U[4096,8192] n_h=32 n_kv=8 D_h=128"
+            " + MLA-absorbed decode 32 seqs x 32768 keys, 128 heads, 576/512 latent")
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -219,8 +225,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
-                               " (oracle: 256 query rows of one (b,h) slice per step)", "l2": "n/a (CPU)"},
+        "config": {"workload": WORKLOAD, "l2": "n/a (host cores)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -389,9 +395,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
-                                   " + GQA decode 59 seqs L~U[4096,8192] n_h=32 n_kv=8 D_h=128"
-                                   " + MLA-absorbed decode 32 seqs x 32768 keys, 128 heads, 576/512 latent",
+            "config": {"workload": WORKLOAD,
                        "l2": "every input larger than L2 (129 MB); no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "parts": {
