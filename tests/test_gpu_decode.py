@@ -109,6 +109,7 @@ MLA_SMALL = [
     (5, 100, 1e4),      # RoPE on the last 64 latent dims
     (40, 64, 0.0),      # many short sequences: key ranges of CTA pairs cross sequence ends
     (1, 2000, 0.0),     # one sequence split over every pair
+    (3, 40000, 1e4),    # several 256-key rounds per pair, with RoPE and a ragged last round
 ]
 
 
@@ -136,6 +137,17 @@ def test_mla_decode_batch_limit(lib, B):
     ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
     assert_parity(out, ref, "bf16", f"mla decode B={B}")
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+def test_mla_shaped_decode_fp32(lib):
+    # the tensor-core MLA kernel is bf16; fp32 inputs of the same shape run on the generic kernel
+    cfg = workloads.config("mla_decode", B=2, max_len=200, len_lo=1, len_hi=200, rope_base=1e4, dtype="f32")
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=13)
+    sl[0] = 1
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "f32", "mla-shaped fp32 decode")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= 1e-4
 
 
 def test_mla_decode_score_spikes(lib):
