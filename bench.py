@@ -13,7 +13,11 @@ in HBM:
 4*B*n_h*S^2*D_h); the decode calls report KV GB/s (algorithmic cache bytes) in
 ``parts``.  Every input is larger than the 129 MB L2, so no flush is needed.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--extras]
+
+--extras prints a different line instead: the calls outside the step (chunked,
+windowed, split-halves-RoPE, MLA and GPT-2-shaped prefill, windowed decode, the
+RoPE pass and the fused KV append), each against its roofline on one GPU.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (each
 step: a block of 256 query rows of one (batch, head) slice of the prefill
@@ -422,6 +426,156 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ extra rows (opt-in)
+def visible_pairs(q_pos, n_keys, window=None, n_sink=0):
+    """(query, key) pairs a causal mask admits for queries at positions q_pos over
+    keys 0..n_keys-1; with a window, key n is visible from m when n <= m and
+    (m - n < window or n < n_sink)."""
+    total = 0
+    for m in q_pos:
+        hi = min(m, n_keys - 1) + 1
+        if window is None:
+            total += hi
+        else:
+            in_win = min(hi, window)
+            total += in_win + min(n_sink, max(0, hi - window))
+    return float(total)
+
+
+def run_extras(args):
+    """One JSON line timing the calls outside the default step, each on its own
+    workload against its roofline.  L2 is flushed (a 256 MB write) before every
+    timed call, outside the events."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_causal_attention_gb300 as attn
+    attn.load()
+    peaks, peak_kind = load_peaks()
+    hbm_peak, bf16_peak = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            total += a.elapsed_time(b)
+        if attn.device_status() != 0:
+            raise RuntimeError("a kernel reported a device-side wait timeout")
+        return total / args.steps
+
+    def tensor_row(name, ms, flops):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"workload": name, "ms": ms, "value": tf, "unit": "TFLOP/s", "bound": "tensor",
+                "frac": tf / bf16_peak}
+
+    def hbm_row(name, ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"workload": name, "ms": ms, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm_peak}
+
+    rows = {}
+    # Llama-3-8B-shaped tensors shared by several rows
+    pc = workloads.config("llama3_8b")
+    q, k, v = (t.to(dev) for t in workloads.prefill_inputs(pc, seed=0))
+    B, S, n_h, n_kv, D = pc["B"], pc["S"], pc["n_h"], pc["n_kv"], pc["D_h"]
+    out, k_rot = torch.empty_like(q), torch.empty_like(k)
+
+    # half-split RoPE pairing on the prefill workload
+    ms = timed(lambda: attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot,
+                                    pairing="half", stream=stream))
+    rows["prefill_half_rope"] = tensor_row("llama3-8b prefill B=4 S=8192, split-halves RoPE pairing", ms,
+                                           workloads.causal_flops(B, S, n_h, D))
+
+    # sliding window of 4096 keys plus 4 sinks on the prefill workload
+    win, sinks = 4096, 4
+    ms = timed(lambda: attn.prefill_window(q, k, v, window=win, n_sink=sinks, rope_base=pc["rope_base"],
+                                           scale=pc["scale"], out=out, k_rot=k_rot, stream=stream))
+    rows["prefill_window"] = tensor_row(
+        f"llama3-8b prefill B=4 S=8192, window {win} + {sinks} sinks", ms,
+        4.0 * D * n_h * B * visible_pairs(range(S), S, win, sinks))
+
+    # chunked prefill: the last 2048 queries at offset 6144 over the 8192-key rotated cache
+    attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot, stream=stream)
+    off, sq = 6144, 2048
+    qc = q[:, off:].contiguous()
+    outc = torch.empty_like(qc)
+    ms = timed(lambda: attn.prefill_chunk(qc, k_rot, v, q_offset=off, rope_base=pc["rope_base"], scale=pc["scale"],
+                                          out=outc, stream=stream))
+    rows["prefill_chunk"] = tensor_row(
+        f"llama3-8b chunk of {sq} queries at offset {off}, B=4, over an 8192-key cache", ms,
+        4.0 * D * n_h * B * visible_pairs(range(off, off + sq), off + sq))
+
+    # the RoPE pass alone, on Q (268 MB in, 268 MB out)
+    qr = torch.empty_like(q)
+    ms = timed(lambda: attn.rope(q, rope_base=pc["rope_base"], out=qr, stream=stream))
+    rows["rope"] = hbm_row("RoPE of llama3-8b Q [4,8192,32,128] bf16", ms, 2.0 * q.numel() * q.element_size())
+    del qr, qc, outc
+
+    # fused RoPE + KV append: an 8192-token prompt per sequence into a 16384-slot cache
+    cap = 2 * S
+    kcache = torch.empty((B, cap, n_kv, D), dtype=k.dtype, device=dev)
+    vcache = torch.empty_like(kcache)
+    start = torch.full((B,), 4096, dtype=torch.int32, device=dev)
+    ms = timed(lambda: attn.kv_append(k, v, kcache, vcache, start, rope_base=pc["rope_base"], stream=stream))
+    rows["kv_append"] = hbm_row("append 8192 new tokens per sequence, B=4 n_kv=8 D=128, RoPE fused", ms,
+                                2.0 * (k.numel() + v.numel()) * k.element_size())
+    del kcache, vcache, q, k, v, out, k_rot
+    torch.cuda.empty_cache()
+
+    # windowed GQA decode on the decode workload
+    gc = workloads.config("gqa_decode")
+    gq_h, gkc_h, gvc_h, gsl_h = workloads.decode_inputs(gc, seed=0)
+    gq, gkc, gvc, gsl = gq_h.to(dev), gkc_h.to(dev), gvc_h.to(dev), gsl_h.to(dev)
+    gws = torch.empty(attn.decode_workspace_size(gc["B"], gc["n_h"], gc["n_kv"], gc["D_qk"], gc["D_v"],
+                                                 gc["max_len"]), dtype=torch.uint8, device=dev)
+    gout = torch.empty(gc["B"], gc["n_h"], gc["D_v"], dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: attn.decode_window(gq, gkc, gvc, gsl, window=win, n_sink=sinks, rope_base=gc["rope_base"],
+                                          rope_dims=gc["rope_dims"], scale=gc["scale"], out=gout, workspace=gws,
+                                          stream=stream))
+    keys = sum(min(L, win) + min(sinks, max(0, L - win)) for L in gsl_h.tolist())
+    rows["decode_window"] = hbm_row(f"GQA decode 59 seqs L~U[4096,8192], window {win} + {sinks} sinks", ms,
+                                    keys * gc["n_kv"] * (gc["D_qk"] + gc["D_v"]) * 2.0)
+    del gq, gkc, gvc, gsl, gws, gout
+    torch.cuda.empty_cache()
+
+    # MLA prefill on the non-absorbed path
+    mc = workloads.config("mla_prefill")
+    mq, mk, mv = (t.to(dev) for t in workloads.mla_prefill_inputs(mc, seed=0))
+    mout, mk_rot = torch.empty_like(mv), torch.empty_like(mk)
+    ms = timed(lambda: attn.prefill_mla(mq, mk, mv, rope_base=mc["rope_base"], rope_offset=mc["rope_offset"],
+                                        rope_dims=mc["rope_dims"], scale=mc["scale"], out=mout, k_rot=mk_rot,
+                                        stream=stream))
+    rows["prefill_mla"] = tensor_row("MLA prefill B=1 S=4096 128 heads, D_qk=192 D_v=128, RoPE on 64 dims", ms,
+                                     workloads.causal_flops(1, mc["S"], mc["n_h"], mc["D_qk"], mc["D_v"]))
+    del mq, mk, mv, mout, mk_rot
+    torch.cuda.empty_cache()
+
+    # GPT-2-small-shaped prefill (D_h = 64, no RoPE)
+    g2 = workloads.config("gpt2")
+    q2, k2, v2 = (t.to(dev) for t in workloads.prefill_inputs(g2, seed=0))
+    out2 = torch.empty_like(q2)
+    ms = timed(lambda: attn.prefill(q2, k2, v2, scale=g2["scale"], out=out2, stream=stream))
+    rows["prefill_gpt2"] = tensor_row("GPT-2-small prefill B=8 S=1024 12 heads D=64", ms,
+                                      workloads.causal_flops(g2["B"], g2["S"], g2["n_h"], g2["D_h"]))
+
+    line = {"impl": "ours", "extras": rows, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+            "data": "synthetic", "l2": "256 MB flush write before every timed call",
+            "peaks": {"bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak, "source": peak_kind}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,6 +586,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--parts", default="prefill,gqa,mla",
                     help="comma-separated subset of prefill,gqa,mla (profiling runs)")
+    ap.add_argument("--extras", action="store_true",
+                    help="time the calls outside the default step instead (separate JSON line)")
     ap.add_argument("--prefill-batch", type=int, default=4,
                     help="batch of the prefill workload (4 = the benchmark workload; smaller for profiling)")
     args = ap.parse_args()
@@ -440,6 +596,8 @@ def main():
     args.parts = [p for p in args.parts.split(",") if p]
     if args.impl == "reference":
         return run_reference(args)
+    if args.extras:
+        return run_extras(args)
     return run_ours(args)
 
 

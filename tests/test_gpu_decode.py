@@ -196,17 +196,16 @@ def test_rows_past_seqlens_are_never_used(lib, name):
     assert_parity(out, ref, "bf16", f"{name} with NaN past seqlens")
 
 
-@pytest.mark.parametrize("name,window,sink", [
-    ("gqa_decode", 1000, 4),
-    ("gqa_decode", 300, 0),
-    ("mla_decode", 500, 4),
+@pytest.mark.parametrize("name,window,sink,B,max_len", [
+    ("gqa_decode", 1000, 4, 4, 3000),     # one chunk per sequence holding both the sinks and the window
+    ("gqa_decode", 300, 0, 4, 3000),
+    ("gqa_decode", 4100, 4, 3, 12000),    # several chunks: sinks alone in one, chunks with neither skipped
+    ("gqa_decode", 4096, 1, 2, 9000),     # window a multiple of the tile
+    ("mla_decode", 500, 4, 2, 1500),
 ])
-def test_decode_sliding_window_with_sinks(lib, name, window, sink):
+def test_decode_sliding_window_with_sinks(lib, name, window, sink, B, max_len):
     # "Transformer 与 LLM" slide 07: keep a window of recent keys plus a few sink tokens
-    if name == "gqa_decode":
-        cfg = workloads.config(name, B=4, max_len=3000, len_lo=1, len_hi=3000)
-    else:
-        cfg = workloads.config(name, B=2, max_len=1500, len_lo=1, len_hi=1500)
+    cfg = workloads.config(name, B=B, max_len=max_len, len_lo=1, len_hi=max_len)
     q, kc, vc, sl = workloads.decode_inputs(cfg, seed=window)
     sl[0] = 2
     sl[-1] = cfg["max_len"]

@@ -463,7 +463,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
         !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, kMlaTileKeys))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);
-  } else if (window == 0 && decode_tc_supported(n_h, n_kv, D_qk, D_v, bf16, rope_offset, rope_dims, rope)) {
+  } else if (decode_tc_supported(n_h, n_kv, D_qk, D_v, bf16, rope_offset, rope_dims, rope)) {
     // K and V tiles of 128 keys on the tensor cores (keys on M, the head group on N)
     CUtensorMap maps[2];
     const unsigned long long ks = static_cast<unsigned long long>(D_qk) * 2;

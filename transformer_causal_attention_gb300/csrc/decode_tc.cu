@@ -29,7 +29,11 @@
 // a global counter (sequence lengths differ, so a static split left the
 // busiest SM 9% above the mean) and hands each to the consumers through a
 // small shared-memory queue.  Each unit writes one normalised partial per
-// head, merged by the combine kernel of decode.cu.
+// head, merged by the combine kernel of decode.cu.  With a sliding window a
+// unit keeps only its chunk's keys inside the window or among the sinks (one
+// or two key ranges, each tiled from its first key), and chunks with none of
+// them are never claimed, so the kernel reads only visible rows (plus the
+// rest of the sinks' one tile).
 #include <math.h>
 
 #include "kernels.h"
@@ -76,22 +80,47 @@ struct Bars {
   int abort_flag;
 };
 
+// A work unit: the visible keys of one chunk of one sequence for one KV head,
+// as one or two key ranges [lo, hi) (two when a chunk holds both the sinks and
+// the start of a sliding window).  Tiles of BK keys start at each range's first
+// key; keys of a tile past its range's end are masked.
 struct Unit {
-  int b, g, start, end, L;
+  int b, g, split, L;
+  int lo[2], hi[2];
+  int nt0, nt;  // tiles of the first range, of both
 };
 
 // Units enumerate (b, chunk, g) with the KV head fastest.  Chunks past the
-// sequence are empty.
+// sequence, or with no key inside the window or the sinks, are empty.
 __device__ __forceinline__ bool unit_at(int u, const DecodeArgs& a, Unit& w) {
   w.g = u % a.n_kv;
   const int r = u / a.n_kv;
-  const int split = r % a.n_split;
+  w.split = r % a.n_split;
   w.b = r / a.n_split;
   w.L = min(max(a.seqlens[w.b], 1), a.max_len);
-  w.start = split * a.chunk;
-  w.end = min(w.L, w.start + a.chunk);
-  return w.start < w.L;
+  const int start = w.split * a.chunk, end = min(w.L, start + a.chunk);
+  int vlo[2], vhi[2];
+  const int nr = decode_visible(w.L, a.window, a.n_sink, vlo, vhi);
+  int n = 0;
+  for (int i = 0; i < nr; ++i) {
+    const int lo = max(start, vlo[i]), hi = min(end, vhi[i]);
+    if (lo < hi) {
+      w.lo[n] = lo;
+      w.hi[n] = hi;
+      ++n;
+    }
+  }
+  if (n == 0) return false;
+  w.nt0 = (w.hi[0] - w.lo[0] + BK - 1) / BK;
+  w.nt = w.nt0 + (n == 2 ? (w.hi[1] - w.lo[1] + BK - 1) / BK : 0);
+  return true;
 }
+
+// First key of tile t of a unit, and the end of the range it belongs to.
+__device__ __forceinline__ int tile_key0(const Unit& w, int t) {
+  return t < w.nt0 ? w.lo[0] + t * BK : w.lo[1] + (t - w.nt0) * BK;
+}
+__device__ __forceinline__ int tile_kend(const Unit& w, int t) { return t < w.nt0 ? w.hi[0] : w.hi[1]; }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const bool ok = mbar_wait(bar, parity, w);
@@ -201,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->unit_full[qs]);
         if (++qs == kUnitSlots) { qs = 0; qph ^= 1; }
         if (u >= n_units) break;
-        for (int k0 = w.start; k0 < w.end; k0 += BK) {
+        for (int t = 0; t < w.nt; ++t) {
+          const int k0 = tile_key0(w, t);
           if (!mbar_wait(&bars->empty[st], ph ^ 1, wc)) goto producer_done;
           mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
           uint8_t* kdst = smem + kKVOff + st * kStageBytes;
@@ -257,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u < 0) break;
         Unit w;
         unit_at(u, a, w);
-        const int nt = (w.end - w.start + BK - 1) / BK;
+        const int nt = w.nt;
         if (!mbar_wait(&bars->q_ready, n & 1, wc)) goto mma_done;
         if (!mbar_wait(&bars->full[st], ph, wc)) goto mma_done;
         tc_fence_after();
@@ -308,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) break;
       Unit w;
       unit_at(u, a, w);
-      const int nt = (w.end - w.start + BK - 1) / BK;
+      const int nt = w.nt;
       const int h0 = w.g * G;
       // Q_g into shared memory (rows = heads, K-major, 128-byte swizzle), rotated at
       // the new token's position; the previous unit's QK MMAs must have finished
@@ -365,8 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[NHP];
         tmem_ld16(tmem + lane_off + sbuf * NHP, sr);
         tmem_wait_ld();
-        const int key = w.start + t * BK + k;
-        const bool valid = key < w.end;
+        const bool valid = tile_key0(w, t) + k < tile_kend(w, t);
         float x[NHP];
 #pragma unroll
         for (int i = 0; i < NHP; ++i) x[i] = valid ? __uint_as_float(sr[i]) * a.scale_log2 : -INFINITY;
@@ -422,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<__nv_bfloat16*>(pb + sw128_off(i, k, kPBlockBytes)) = __float2bfloat16_rn(p);
         }
         if (!valid) {
-          // rows past the chunk may hold anything (even NaN): zero this key's value row so
+          // rows past the range may hold anything (even NaN): zero this key's value row so
           // that P V stays finite
           uint8_t* vt = smem + kKVOff + st * kStageBytes + kTileBytes;
 #pragma unroll
@@ -454,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
-      const int split = w.start / a.chunk;
+      const int split = w.split;
 #pragma unroll
       for (int i = 0; i < NHP; ++i) {
         if (i >= G) break;

@@ -132,9 +132,17 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
       const int d0 = (ch - kch) * 8;
       const T* src = static_cast<const T*>(a.v_new) + (bc * a.n_kv) * a.D_v + d0;
       T* dst = static_cast<T*>(a.vcache) + slot * a.v_token_stride + d0;
-      for (int h = 0; h < a.n_kv; ++h)
+      if (a.v_token_stride % 8 == 0) {  // every value chunk starts on a 16-byte boundary: copy whole chunks
+        for (int h = 0; h < a.n_kv; ++h) {
+          float x[8];
+          load_chunk<T, 8>(src + h * a.D_v, x);
+          store_chunk<T, 8>(dst + h * a.D_v, x);
+        }
+      } else {
+        for (int h = 0; h < a.n_kv; ++h)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dst[h * a.D_v + e] = src[h * a.D_v + e];
+          for (int e = 0; e < 8; ++e) dst[h * a.D_v + e] = src[h * a.D_v + e];
+      }
     }
   }
 }
