@@ -28,6 +28,7 @@ struct PrefillArgs {
   int n_sink;        // ... plus the first n_sink keys (attention sinks); window 0: no window
   int D_v;           // head dim of v and out
   int rope_offset;   // first rotated dim of q and k (the span holds 2 * n_pairs dims)
+  int fold;          // 1: deal work items as (heavy, light) pairs of one head, head after head
 };
 
 struct DecodeArgs {

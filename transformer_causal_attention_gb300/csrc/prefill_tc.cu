@@ -138,16 +138,33 @@ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, in
 // of gridDim.x, every other wave in reverse CTA order, so that no CTA takes the heaviest item of
 // every wave (with one direction only, the busiest CTA of the Llama-3-8B prefill would carry
 // 3.5% more key tiles than the mean; alternating brings that to 0.1%).
+// Folded dealing instead hands each CTA double items: the tile pairs p and n_pairs - 1 - p of
+// one (batch, head), heavy one first, which together always hold the same number of key
+// tiles; double items go out head after head, so the CTAs running at one time share few K/V
+// heads and their key tiles are re-read from L2 rather than HBM.
+// The dealing is a template parameter: a run-time switch here cost the Llama-3-8B
+// prefill 2.7% (register spills in the item loops).
+template <bool FOLD>
 __device__ __forceinline__ int item_at(uint32_t k) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if constexpr (FOLD) return 2 * (static_cast<int>(k >> 1) * g + c) + static_cast<int>(k & 1u);
   return static_cast<int>(k) * g + ((k & 1u) ? g - 1 - c : c);
 }
 
+template <bool FOLD>
 __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n_pairs_q, int n_kt) {
   Item it;
-  const int bh_count = a.B * a.n_h;
-  const int p = n_pairs_q - 1 - idx / bh_count;  // heaviest (latest) tile pairs first
-  const int bh = idx % bh_count;
+  int p, bh;
+  if constexpr (FOLD) {  // n_pairs_q is even
+    const unsigned half = static_cast<unsigned>(n_pairs_q) >> 1, d = static_cast<unsigned>(idx) >> 1;
+    bh = static_cast<int>(d / half);
+    const int j = static_cast<int>(d - static_cast<unsigned>(bh) * half);
+    p = (idx & 1) ? j : n_pairs_q - 1 - j;
+  } else {
+    const int bh_count = a.B * a.n_h;
+    p = n_pairs_q - 1 - idx / bh_count;  // heaviest (latest) tile pairs first
+    bh = idx % bh_count;
+  }
   it.b = bh / a.n_h;
   it.h = bh % a.n_h;
   it.g = it.h / (a.n_h / a.n_kv);
@@ -226,7 +243,7 @@ __device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope
   }
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool FOLD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -304,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t st = 0, ph = 0;
         uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
         uint32_t q_issued = 0, it = 0;
-        for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
-          const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
+        for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
+          const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           if (is_v) {
             for (int t = 0; t < 2; ++t) {
               if (!mbar_wait(&bars->q_empty[t], (it & 1) ^ 1, wc)) goto load_done;
@@ -364,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
-          const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
+        for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
+          const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
           if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
           {
@@ -442,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + C::kOCol0 + (t ? DV : 0);
     uint32_t sph = 0;
     uint32_t it = 0;
-    for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
-      const Item itm = decode_item(idx, a, n_pairs_q, n_kt);
+    for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
+      const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
       const TileRange rng = t ? itm.r1 : itm.r0;
       const int n_t = rng.count();
@@ -598,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 // Per head-dim pair, one bit per device that has been prepared.
-std::atomic<unsigned> g_ready[3];
+std::atomic<unsigned> g_ready[5];
 
 // Opt in to the kernel's shared memory and check, once per process and device,
 // that the compiled kernel holds enough registers per thread for its register
@@ -619,10 +636,10 @@ cudaError_t prepare(K kernel, int smem_bytes, std::atomic<unsigned>* ready) {
   return cudaSuccess;
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool FOLD = false>
 cudaError_t launch(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int grid, cudaStream_t st,
                    std::atomic<unsigned>* ready) {
-  auto k = prefill_tc_kernel<DQK, DV>;
+  auto k = prefill_tc_kernel<DQK, DV, FOLD>;
   const cudaError_t e = prepare(k, Cfg<DQK, DV>::kSmemBytes, ready);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, Cfg<DQK, DV>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
@@ -640,12 +657,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const 
   const long long n_items = static_cast<long long>(a.B) * a.n_h * ((n_qt + 1) / 2);
   const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
   cudaError_t e;
+  // folded dealing is built for the two larger head dims (D = 64 prompts whose K/V
+  // pass twice the L2 take the plain dealing)
   if (a.D == 64)
     e = launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
   else if (a.D == 128)
-    e = launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
+    e = a.fold ? launch<128, 128, true>(a, rope, maps, grid, st, &g_ready[3])
+               : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
   else
-    e = launch<192, 128>(a, rope, maps, grid, st, &g_ready[2]);
+    e = a.fold ? launch<192, 128, true>(a, rope, maps, grid, st, &g_ready[4])
+               : launch<192, 128>(a, rope, maps, grid, st, &g_ready[2]);
   *launches += 1;
   return e;
 }
