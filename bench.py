@@ -48,7 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # DRAM bytes (read + write) per launch of the prefill kernel, from the ncu
 # capture summarised in profiles/prefill_tc_llama3_8b.md, valid only for the
 # kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits).
-PREFILL_TRAFFIC = {"kernel_sha": "dd87d4970ff1c79c", "bytes": 4 * 128.293e6}
+PREFILL_TRAFFIC = {"kernel_sha": "625f28560df910fe", "bytes": 4 * 128.286e6}
 
 
 def kernel_sha(name: str) -> str:
@@ -175,7 +175,7 @@ def sample_rows(cfg, i, n_rows=256):
     return b, h, list(range(r0, r0 + n_rows))
 
 
-def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 12.0, max_samples: int = 64):
+def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 12.0, max_samples: int = 512):
     done, secs, flops = 0, 0.0, 0.0
     while done < max_samples and (done == 0 or secs < budget_s):
         b, h, rows = sample_rows(cfg, done)
@@ -485,89 +485,100 @@ def run_extras(args):
         return {"workload": name, "ms": ms, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm_peak}
 
     rows = {}
-    # Llama-3-8B-shaped tensors shared by several rows
-    pc = workloads.config("llama3_8b")
-    q, k, v = (t.to(dev) for t in workloads.prefill_inputs(pc, seed=0))
-    B, S, n_h, n_kv, D = pc["B"], pc["S"], pc["n_h"], pc["n_kv"], pc["D_h"]
-    out, k_rot = torch.empty_like(q), torch.empty_like(k)
-
-    # half-split RoPE pairing on the prefill workload
-    ms = timed(lambda: attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot,
-                                    pairing="half", stream=stream))
-    rows["prefill_half_rope"] = tensor_row("llama3-8b prefill B=4 S=8192, split-halves RoPE pairing", ms,
-                                           workloads.causal_flops(B, S, n_h, D))
-
-    # sliding window of 4096 keys plus 4 sinks on the prefill workload
     win, sinks = 4096, 4
-    ms = timed(lambda: attn.prefill_window(q, k, v, window=win, n_sink=sinks, rope_base=pc["rope_base"],
-                                           scale=pc["scale"], out=out, k_rot=k_rot, stream=stream))
-    rows["prefill_window"] = tensor_row(
-        f"llama3-8b prefill B=4 S=8192, window {win} + {sinks} sinks", ms,
-        4.0 * D * n_h * B * visible_pairs(range(S), S, win, sinks))
 
-    # chunked prefill: the last 2048 queries at offset 6144 over the 8192-key rotated cache
-    attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot, stream=stream)
-    off, sq = 6144, 2048
-    qc = q[:, off:].contiguous()
-    outc = torch.empty_like(qc)
-    ms = timed(lambda: attn.prefill_chunk(qc, k_rot, v, q_offset=off, rope_base=pc["rope_base"], scale=pc["scale"],
-                                          out=outc, stream=stream))
-    rows["prefill_chunk"] = tensor_row(
-        f"llama3-8b chunk of {sq} queries at offset {off}, B=4, over an 8192-key cache", ms,
-        4.0 * D * n_h * B * visible_pairs(range(off, off + sq), off + sq))
+    host = {}
 
-    # the RoPE pass alone, on Q (268 MB in, 268 MB out)
-    qr = torch.empty_like(q)
-    ms = timed(lambda: attn.rope(q, rope_base=pc["rope_base"], out=qr, stream=stream))
-    rows["rope"] = hbm_row("RoPE of llama3-8b Q [4,8192,32,128] bf16", ms, 2.0 * q.numel() * q.element_size())
-    del qr, qc, outc
+    def llama_inputs():
+        pc = workloads.config("llama3_8b")
+        if "llama" not in host:  # drawn once on the CPU, copied to the device for each row
+            host["llama"] = workloads.prefill_inputs(pc, seed=0)
+        q, k, v = (t.to(dev) for t in host["llama"])
+        return pc, q, k, v, torch.empty_like(q), torch.empty_like(k)
 
-    # fused RoPE + KV append: an 8192-token prompt per sequence into a 16384-slot cache
-    cap = 2 * S
-    kcache = torch.empty((B, cap, n_kv, D), dtype=k.dtype, device=dev)
-    vcache = torch.empty_like(kcache)
-    start = torch.full((B,), 4096, dtype=torch.int32, device=dev)
-    ms = timed(lambda: attn.kv_append(k, v, kcache, vcache, start, rope_base=pc["rope_base"], stream=stream))
-    rows["kv_append"] = hbm_row("append 8192 new tokens per sequence, B=4 n_kv=8 D=128, RoPE fused", ms,
-                                2.0 * (k.numel() + v.numel()) * k.element_size())
-    del kcache, vcache, q, k, v, out, k_rot
-    torch.cuda.empty_cache()
+    def prefill_half_rope():  # split-halves RoPE pairing on the prefill workload
+        pc, q, k, v, out, k_rot = llama_inputs()
+        ms = timed(lambda: attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out,
+                                        k_rot=k_rot, pairing="half", stream=stream))
+        return tensor_row("llama3-8b prefill B=4 S=8192, split-halves RoPE pairing", ms,
+                          workloads.causal_flops(pc["B"], pc["S"], pc["n_h"], pc["D_h"]))
 
-    # windowed GQA decode on the decode workload
-    gc = workloads.config("gqa_decode")
-    gq_h, gkc_h, gvc_h, gsl_h = workloads.decode_inputs(gc, seed=0)
-    gq, gkc, gvc, gsl = gq_h.to(dev), gkc_h.to(dev), gvc_h.to(dev), gsl_h.to(dev)
-    gws = torch.empty(attn.decode_workspace_size(gc["B"], gc["n_h"], gc["n_kv"], gc["D_qk"], gc["D_v"],
-                                                 gc["max_len"]), dtype=torch.uint8, device=dev)
-    gout = torch.empty(gc["B"], gc["n_h"], gc["D_v"], dtype=torch.bfloat16, device=dev)
-    ms = timed(lambda: attn.decode_window(gq, gkc, gvc, gsl, window=win, n_sink=sinks, rope_base=gc["rope_base"],
-                                          rope_dims=gc["rope_dims"], scale=gc["scale"], out=gout, workspace=gws,
-                                          stream=stream))
-    keys = sum(min(L, win) + min(sinks, max(0, L - win)) for L in gsl_h.tolist())
-    rows["decode_window"] = hbm_row(f"GQA decode 59 seqs L~U[4096,8192], window {win} + {sinks} sinks", ms,
-                                    keys * gc["n_kv"] * (gc["D_qk"] + gc["D_v"]) * 2.0)
-    del gq, gkc, gvc, gsl, gws, gout
-    torch.cuda.empty_cache()
+    def prefill_window():  # sliding window of 4096 keys plus 4 sinks on the prefill workload
+        pc, q, k, v, out, k_rot = llama_inputs()
+        ms = timed(lambda: attn.prefill_window(q, k, v, window=win, n_sink=sinks, rope_base=pc["rope_base"],
+                                               scale=pc["scale"], out=out, k_rot=k_rot, stream=stream))
+        return tensor_row(f"llama3-8b prefill B=4 S=8192, window {win} + {sinks} sinks", ms,
+                          4.0 * pc["D_h"] * pc["n_h"] * pc["B"] * visible_pairs(range(pc["S"]), pc["S"], win, sinks))
 
-    # MLA prefill on the non-absorbed path
-    mc = workloads.config("mla_prefill")
-    mq, mk, mv = (t.to(dev) for t in workloads.mla_prefill_inputs(mc, seed=0))
-    mout, mk_rot = torch.empty_like(mv), torch.empty_like(mk)
-    ms = timed(lambda: attn.prefill_mla(mq, mk, mv, rope_base=mc["rope_base"], rope_offset=mc["rope_offset"],
-                                        rope_dims=mc["rope_dims"], scale=mc["scale"], out=mout, k_rot=mk_rot,
-                                        stream=stream))
-    rows["prefill_mla"] = tensor_row("MLA prefill B=1 S=4096 128 heads, D_qk=192 D_v=128, RoPE on 64 dims", ms,
-                                     workloads.causal_flops(1, mc["S"], mc["n_h"], mc["D_qk"], mc["D_v"]))
-    del mq, mk, mv, mout, mk_rot
-    torch.cuda.empty_cache()
+    def prefill_chunk():  # the last 2048 queries at offset 6144 over the 8192-key rotated cache
+        pc, q, k, v, out, k_rot = llama_inputs()
+        attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot, stream=stream)
+        off, sq = 6144, 2048
+        qc = q[:, off:].contiguous()
+        outc = torch.empty_like(qc)
+        ms = timed(lambda: attn.prefill_chunk(qc, k_rot, v, q_offset=off, rope_base=pc["rope_base"],
+                                              scale=pc["scale"], out=outc, stream=stream))
+        return tensor_row(f"llama3-8b chunk of {sq} queries at offset {off}, B=4, over an 8192-key cache", ms,
+                          4.0 * pc["D_h"] * pc["n_h"] * pc["B"] * visible_pairs(range(off, off + sq), off + sq))
 
-    # GPT-2-small-shaped prefill (D_h = 64, no RoPE)
-    g2 = workloads.config("gpt2")
-    q2, k2, v2 = (t.to(dev) for t in workloads.prefill_inputs(g2, seed=0))
-    out2 = torch.empty_like(q2)
-    ms = timed(lambda: attn.prefill(q2, k2, v2, scale=g2["scale"], out=out2, stream=stream))
-    rows["prefill_gpt2"] = tensor_row("GPT-2-small prefill B=8 S=1024 12 heads D=64", ms,
-                                      workloads.causal_flops(g2["B"], g2["S"], g2["n_h"], g2["D_h"]))
+    def rope():  # the RoPE pass alone, on Q (268 MB in, 268 MB out)
+        pc, q, _, _, qr, _ = llama_inputs()
+        ms = timed(lambda: attn.rope(q, rope_base=pc["rope_base"], out=qr, stream=stream))
+        return hbm_row("RoPE of llama3-8b Q [4,8192,32,128] bf16", ms, 2.0 * q.numel() * q.element_size())
+
+    def kv_append():  # fused RoPE + KV append: an 8192-token prompt per sequence into a 16384-slot cache
+        pc, _, k, v, _, _ = llama_inputs()
+        B, S, n_kv, D = pc["B"], pc["S"], pc["n_kv"], pc["D_h"]
+        kcache = torch.empty((B, 2 * S, n_kv, D), dtype=k.dtype, device=dev)
+        vcache = torch.empty_like(kcache)
+        start = torch.full((B,), 4096, dtype=torch.int32, device=dev)
+        ms = timed(lambda: attn.kv_append(k, v, kcache, vcache, start, rope_base=pc["rope_base"], stream=stream))
+        return hbm_row("append 8192 new tokens per sequence, B=4 n_kv=8 D=128, RoPE fused", ms,
+                       2.0 * (k.numel() + v.numel()) * k.element_size())
+
+    def decode_window():  # windowed GQA decode on the decode workload
+        gc = workloads.config("gqa_decode")
+        gq_h, gkc_h, gvc_h, gsl_h = workloads.decode_inputs(gc, seed=0)
+        gq, gkc, gvc, gsl = gq_h.to(dev), gkc_h.to(dev), gvc_h.to(dev), gsl_h.to(dev)
+        gws = torch.empty(attn.decode_workspace_size(gc["B"], gc["n_h"], gc["n_kv"], gc["D_qk"], gc["D_v"],
+                                                     gc["max_len"]), dtype=torch.uint8, device=dev)
+        gout = torch.empty(gc["B"], gc["n_h"], gc["D_v"], dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: attn.decode_window(gq, gkc, gvc, gsl, window=win, n_sink=sinks,
+                                              rope_base=gc["rope_base"], rope_dims=gc["rope_dims"],
+                                              scale=gc["scale"], out=gout, workspace=gws, stream=stream))
+        keys = sum(min(L, win) + min(sinks, max(0, L - win)) for L in gsl_h.tolist())
+        return hbm_row(f"GQA decode 59 seqs L~U[4096,8192], window {win} + {sinks} sinks", ms,
+                       keys * gc["n_kv"] * (gc["D_qk"] + gc["D_v"]) * 2.0)
+
+    def prefill_mla():  # MLA prefill on the non-absorbed path
+        mc = workloads.config("mla_prefill")
+        mq, mk, mv = (t.to(dev) for t in workloads.mla_prefill_inputs(mc, seed=0))
+        mout, mk_rot = torch.empty_like(mv), torch.empty_like(mk)
+        ms = timed(lambda: attn.prefill_mla(mq, mk, mv, rope_base=mc["rope_base"], rope_offset=mc["rope_offset"],
+                                            rope_dims=mc["rope_dims"], scale=mc["scale"], out=mout, k_rot=mk_rot,
+                                            stream=stream))
+        return tensor_row("MLA prefill B=1 S=4096 128 heads, D_qk=192 D_v=128, RoPE on 64 dims", ms,
+                          workloads.causal_flops(1, mc["S"], mc["n_h"], mc["D_qk"], mc["D_v"]))
+
+    def prefill_gpt2():  # GPT-2-small-shaped prefill (D_h = 64, no RoPE)
+        g2 = workloads.config("gpt2")
+        q2, k2, v2 = (t.to(dev) for t in workloads.prefill_inputs(g2, seed=0))
+        out2 = torch.empty_like(q2)
+        ms = timed(lambda: attn.prefill(q2, k2, v2, scale=g2["scale"], out=out2, stream=stream))
+        return tensor_row("GPT-2-small prefill B=8 S=1024 12 heads D=64", ms,
+                          workloads.causal_flops(g2["B"], g2["S"], g2["n_h"], g2["D_h"]))
+
+    table = [("prefill_half_rope", prefill_half_rope), ("prefill_window", prefill_window),
+             ("prefill_chunk", prefill_chunk), ("rope", rope), ("kv_append", kv_append),
+             ("decode_window", decode_window), ("prefill_mla", prefill_mla), ("prefill_gpt2", prefill_gpt2)]
+    want = set(args.rows.split(",")) if args.rows else {name for name, _ in table}
+    unknown = want - {name for name, _ in table}
+    if unknown:
+        raise SystemExit(f"unknown rows: {sorted(unknown)}")
+    for name, fn in table:
+        if name in want:
+            rows[name] = fn()
+            torch.cuda.empty_cache()
 
     line = {"impl": "ours", "extras": rows, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
             "data": "synthetic", "l2": "256 MB flush write before every timed call",
@@ -588,6 +599,8 @@ def main():
                     help="comma-separated subset of prefill,gqa,mla (profiling runs)")
     ap.add_argument("--extras", action="store_true",
                     help="time the calls outside the default step instead (separate JSON line)")
+    ap.add_argument("--rows", default="",
+                    help="with --extras: comma-separated subset of its rows (profiling runs)")
     ap.add_argument("--prefill-batch", type=int, default=4,
                     help="batch of the prefill workload (4 = the benchmark workload; smaller for profiling)")
     args = ap.parse_args()

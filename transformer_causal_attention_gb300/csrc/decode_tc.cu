@@ -86,12 +86,13 @@ struct Bars {
 // key; keys of a tile past its range's end are masked.
 struct Unit {
   int b, g, split, L;
-  int lo[2], hi[2];
-  int nt0, nt;  // tiles of the first range, of both
+  int lo0, hi0, lo1, hi1;  // the key ranges (the second one empty unless nt > nt0)
+  int nt0, nt;             // tiles of the first range, of both
 };
 
 // Units enumerate (b, chunk, g) with the KV head fastest.  Chunks past the
-// sequence, or with no key inside the window or the sinks, are empty.
+// sequence, or with no key inside the window or the sinks, are empty.  (Scalar
+// fields, not arrays: a runtime-indexed array would live in local memory.)
 __device__ __forceinline__ bool unit_at(int u, const DecodeArgs& a, Unit& w) {
   w.g = u % a.n_kv;
   const int r = u / a.n_kv;
@@ -99,28 +100,38 @@ __device__ __forceinline__ bool unit_at(int u, const DecodeArgs& a, Unit& w) {
   w.b = r / a.n_split;
   w.L = min(max(a.seqlens[w.b], 1), a.max_len);
   const int start = w.split * a.chunk, end = min(w.L, start + a.chunk);
-  int vlo[2], vhi[2];
-  const int nr = decode_visible(w.L, a.window, a.n_sink, vlo, vhi);
   int n = 0;
-  for (int i = 0; i < nr; ++i) {
-    const int lo = max(start, vlo[i]), hi = min(end, vhi[i]);
-    if (lo < hi) {
-      w.lo[n] = lo;
-      w.hi[n] = hi;
-      ++n;
+  w.lo0 = w.hi0 = w.lo1 = w.hi1 = 0;
+  auto add = [&](int vlo, int vhi) {  // keep [vlo, vhi) within the chunk
+    const int lo = max(start, vlo), hi = min(end, vhi);
+    if (lo >= hi) return;
+    if (n == 0) {
+      w.lo0 = lo;
+      w.hi0 = hi;
+    } else {
+      w.lo1 = lo;
+      w.hi1 = hi;
     }
+    ++n;
+  };
+  // the visible keys of the new token at position L - 1 (decode_visible in kernels.h)
+  if (a.window <= 0 || w.L - a.window <= a.n_sink) {
+    add(0, w.L);
+  } else {
+    if (a.n_sink > 0) add(0, a.n_sink);
+    add(w.L - a.window, w.L);
   }
   if (n == 0) return false;
-  w.nt0 = (w.hi[0] - w.lo[0] + BK - 1) / BK;
-  w.nt = w.nt0 + (n == 2 ? (w.hi[1] - w.lo[1] + BK - 1) / BK : 0);
+  w.nt0 = (w.hi0 - w.lo0 + BK - 1) / BK;
+  w.nt = w.nt0 + (n == 2 ? (w.hi1 - w.lo1 + BK - 1) / BK : 0);
   return true;
 }
 
 // First key of tile t of a unit, and the end of the range it belongs to.
 __device__ __forceinline__ int tile_key0(const Unit& w, int t) {
-  return t < w.nt0 ? w.lo[0] + t * BK : w.lo[1] + (t - w.nt0) * BK;
+  return t < w.nt0 ? w.lo0 + t * BK : w.lo1 + (t - w.nt0) * BK;
 }
-__device__ __forceinline__ int tile_kend(const Unit& w, int t) { return t < w.nt0 ? w.hi[0] : w.hi[1]; }
+__device__ __forceinline__ int tile_kend(const Unit& w, int t) { return t < w.nt0 ? w.hi0 : w.hi1; }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const bool ok = mbar_wait(bar, parity, w);
