@@ -17,7 +17,8 @@ in HBM:
 
 --extras prints a different line instead: the calls outside the step (chunked,
 windowed, split-halves-RoPE, MLA and GPT-2-shaped prefill, windowed decode, the
-RoPE pass and the fused KV append), each against its roofline on one GPU.
+RoPE pass, the fused KV append, and whole decode steps that append the new
+token before attending), each against its roofline on one GPU.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (each
 step: a block of 256 query rows of one (batch, head) slice of the prefill
@@ -550,6 +551,41 @@ def run_extras(args):
         return hbm_row(f"GQA decode 59 seqs L~U[4096,8192], window {win} + {sinks} sinks", ms,
                        keys * gc["n_kv"] * (gc["D_qk"] + gc["D_v"]) * 2.0)
 
+    def decode_step(name):
+        """One decode step: the new token's key (and value) appended to the cache at slot
+        seqlens[b] - 1 (RoPE fused where the configuration rotates), then attention over the
+        cache.  GB/s over the decode's cache bytes plus the append's bytes; the append alone
+        is reported in microseconds."""
+        cfg = workloads.config(name)
+        q_h, kc_h, vc_h, sl_h = workloads.decode_inputs(cfg, seed=0)
+        q, kc, sl = q_h.to(dev), kc_h.to(dev), sl_h.to(dev)
+        alias = cfg.get("v_aliases_k")
+        vc = kc[..., :cfg["D_v"]] if alias else vc_h.to(dev)
+        g = torch.Generator().manual_seed(1)
+        B, n_kv, D_qk, D_v = cfg["B"], cfg["n_kv"], cfg["D_qk"], cfg["D_v"]
+        k_new = torch.randn((B, 1, n_kv, D_qk), generator=g).to(torch.bfloat16).to(dev)
+        v_new = None if alias else torch.randn((B, 1, n_kv, D_v), generator=g).to(torch.bfloat16).to(dev)
+        start = (sl - 1).to(torch.int32)
+        ws = torch.empty(attn.decode_workspace_size(B, cfg["n_h"], n_kv, D_qk, D_v, cfg["max_len"]),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty(B, cfg["n_h"], D_v, dtype=torch.bfloat16, device=dev)
+        rk = dict(rope_base=cfg["rope_base"], rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"])
+
+        def append():
+            attn.kv_append(k_new, v_new, kc, vc, start, stream=stream, **rk)
+
+        def step():
+            append()
+            attn.decode(q, kc, vc, sl, scale=cfg["scale"], out=out, workspace=ws, stream=stream, **rk)
+
+        ms_append = timed(append)
+        ms = timed(step)
+        new_bytes = 2.0 * B * n_kv * (D_qk + (0 if alias else D_v)) * 2  # read and written once
+        row = hbm_row(f"{name} step: append 1 new token per sequence, then decode", ms,
+                      workloads.decode_bytes(cfg, sl_h.tolist()) + new_bytes)
+        row["kv_append_us"] = ms_append * 1e3
+        return row
+
     def prefill_mla():  # MLA prefill on the non-absorbed path
         mc = workloads.config("mla_prefill")
         mq, mk, mv = (t.to(dev) for t in workloads.mla_prefill_inputs(mc, seed=0))
@@ -570,7 +606,9 @@ def run_extras(args):
 
     table = [("prefill_half_rope", prefill_half_rope), ("prefill_window", prefill_window),
              ("prefill_chunk", prefill_chunk), ("rope", rope), ("kv_append", kv_append),
-             ("decode_window", decode_window), ("prefill_mla", prefill_mla), ("prefill_gpt2", prefill_gpt2)]
+             ("decode_window", decode_window), ("decode_step_gqa", lambda: decode_step("gqa_decode")),
+             ("decode_step_mla", lambda: decode_step("mla_decode")), ("prefill_mla", prefill_mla),
+             ("prefill_gpt2", prefill_gpt2)]
     want = set(args.rows.split(",")) if args.rows else {name for name, _ in table}
     unknown = want - {name for name, _ in table}
     if unknown:

@@ -40,7 +40,8 @@ def make_cache(lib, k, v, max_len, base):
 @pytest.mark.parametrize("B,S,n_h,n_kv,D,dtype,base", [
     (2, 300, 4, 2, 128, "bf16", 5e5),
     (1, 77, 2, 1, 64, "bf16", 1e4),
-    (1, 50, 5, 5, 64, "bf16", 1e4),      # heads not a multiple of the four moved per step
+    (1, 50, 5, 5, 64, "bf16", 1e4),      # a head count that is not a power of two
+    (4, 5000, 8, 8, 128, "bf16", 5e5),   # enough tokens for one thread per (token, chunk) over all heads
     (2, 40, 2, 2, 8, "f32", 1e4),
 ])
 def test_kv_append_writes_rotated_keys(lib, B, S, n_h, n_kv, D, dtype, base):

@@ -103,3 +103,22 @@ def test_mla_prefill_config_full_sampled_rows(lib):
                                                      rope_dims=cfg["rope_dims"])
         assert_parity(out[b, rows, h], ref, "bf16", f"mla prefill (b={b}, h={h})")
         assert np.max(np.abs(to_np(lse[b, h, rows]) - ref_lse)) <= BF16_MAX_ABS
+
+
+def test_mla_prefill_folded_dealing_over_a_batch(lib):
+    # K/V of 2 x 128 heads x 2048 keys (335 MB) is over twice the L2, so the work items are dealt
+    # as (heavy, light) pairs of one head; every item of both sequences must still be computed once
+    cfg = workloads.config("mla_prefill", B=2, S=2048)
+    q, k, v = workloads.mla_prefill_inputs(cfg, seed=5)
+    out, _, lse = lib.prefill_mla(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
+                                  rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
+                                  lse=True)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    rows = np.array([0, 255, 256, 1023, 1024, 1791, 1792, 2047])  # first and last rows of light and heavy pairs
+    for b, h in ((0, 0), (0, 100), (1, 3), (1, 127)):
+        ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, rows, rope_base=cfg["rope_base"],
+                                                     scale=cfg["scale"], rope_offset=cfg["rope_offset"],
+                                                     rope_dims=cfg["rope_dims"])
+        assert_parity(out[b, rows, h], ref, "bf16", f"folded mla prefill (b={b}, h={h})")
+        assert np.max(np.abs(to_np(lse[b, h, rows]) - ref_lse)) <= BF16_MAX_ABS

@@ -244,52 +244,94 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a, Ro
   }
 }
 
+// Four consecutive fp32 values stored as T.
 template <typename T>
-__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeArgs a) {
-  __shared__ float w_s[1024];
-  __shared__ float stat[2];
-  const int bh = blockIdx.x;
+__device__ __forceinline__ void store4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// One warp per (sequence b, head h): the chunk partials' maximum and weight sum by
+// shuffles, then D_v output dims as 16-byte loads of the partials (4 dims per lane per
+// step).  No block-wide step, so the warps of a block never wait for one another.
+constexpr int kCombineWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (bh >= a.B * a.n_h) return;  // whole warps only
   const int b = bh / a.n_h;
   const int L = min(max(a.seqlens[b], 1), a.max_len);
   const int ns = (L + a.chunk - 1) / a.chunk;
   const float* lse = a.ws_lse + static_cast<long long>(bh) * a.n_split;
-  int vlo[2], vhi[2];
-  const int nr = decode_visible(L, a.window, a.n_sink, vlo, vhi);
-  auto written = [&](int j) {  // chunk j holds a visible key, so its partial was written
-    bool any = false;
-    for (int r = 0; r < nr; ++r) any |= max(j * a.chunk, vlo[r]) < min(min(L, (j + 1) * a.chunk), vhi[r]);
-    return any;
-  };
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    for (int j = threadIdx.x; j < ns; j += 32)
-      if (written(j)) M = fmaxf(M, lse[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    for (int j = threadIdx.x; j < ns; j += 32) {
-      const float w = written(j) ? exp2f(lse[j] - M) : 0.f;
-      w_s[j] = w;
-      den += w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (threadIdx.x == 0) {
-      stat[0] = M;
-      stat[1] = den;
+  int lo0, hi0, lo1 = 0, hi1 = 0;
+  {
+    int vlo[2], vhi[2];
+    const int nr = decode_visible(L, a.window, a.n_sink, vlo, vhi);
+    lo0 = vlo[0];
+    hi0 = vhi[0];
+    if (nr == 2) {
+      lo1 = vlo[1];
+      hi1 = vhi[1];
     }
   }
-  __syncthreads();
-  const float inv = 1.f / stat[1];
+  auto written = [&](int j) {  // chunk j holds a visible key, so its partial was written
+    const int c0 = j * a.chunk, c1 = min(L, (j + 1) * a.chunk);
+    return max(c0, lo0) < min(c1, hi0) || max(c0, lo1) < min(c1, hi1);
+  };
+  float M = -INFINITY;
+  for (int j = lane; j < ns; j += 32)
+    if (written(j)) M = fmaxf(M, lse[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float* po = a.ws_o + static_cast<long long>(bh) * a.n_split * a.D_v;
   T* out = static_cast<T*>(a.out) + static_cast<long long>(bh) * a.D_v;
-  for (int d = threadIdx.x; d < a.D_v; d += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < ns; ++j)
-      if (w_s[j] != 0.f) acc = fmaf(w_s[j], po[static_cast<long long>(j) * a.D_v + d], acc);
-    out[d] = from_f32<T>(acc * inv);
+  float den = 0.f;
+  // dims d0 = 4 lane + 128 c; D_v <= 512, a multiple of 8
+  float4 acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < ns; j0 += 32) {
+    const float wl = (j0 + lane < ns && written(j0 + lane)) ? exp2f(lse[j0 + lane] - M) : 0.f;
+    den += wl;
+    const int nj = min(32, ns - j0);
+    for (int jj = 0; jj < nj; ++jj) {
+      const float w = __shfl_sync(0xffffffffu, wl, jj);
+      if (w == 0.f) continue;  // uniform across the warp
+      const float* pj = po + static_cast<long long>(j0 + jj) * a.D_v;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d0 = 4 * lane + 128 * c;
+        if (d0 < a.D_v) {
+          const float4 v = *reinterpret_cast<const float4*>(pj + d0);
+          acc[c].x = fmaf(w, v.x, acc[c].x);
+          acc[c].y = fmaf(w, v.y, acc[c].y);
+          acc[c].z = fmaf(w, v.z, acc[c].z);
+          acc[c].w = fmaf(w, v.w, acc[c].w);
+        }
+      }
+    }
   }
-  if (a.lse != nullptr && threadIdx.x == 0) a.lse[bh] = (stat[0] + log2f(stat[1])) * 0.69314718055994530942f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = 1.f / den;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int d0 = 4 * lane + 128 * c;
+    if (d0 < a.D_v)
+      store4<T>(out + d0, make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv));
+  }
+  if (a.lse != nullptr && lane == 0) a.lse[bh] = (M + log2f(den)) * 0.69314718055994530942f;
 }
 
 // Query heads per CTA: more heads share each loaded K/V row, but every head
@@ -353,10 +395,11 @@ int decode_plan_splits(int B, int n_h, int n_kv, int D_qk, int D_v, int max_len,
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, bool bf16, cudaStream_t st, int* launches) {
+  const unsigned grid = static_cast<unsigned>((a.B * a.n_h + kCombineWarps - 1) / kCombineWarps);
   if (bf16)
-    decode_combine_kernel<__nv_bfloat16><<<a.B * a.n_h, 128, 0, st>>>(a);
+    decode_combine_kernel<__nv_bfloat16><<<grid, kCombineWarps * 32, 0, st>>>(a);
   else
-    decode_combine_kernel<float><<<a.B * a.n_h, 128, 0, st>>>(a);
+    decode_combine_kernel<float><<<grid, kCombineWarps * 32, 0, st>>>(a);
   *launches += 1;
   return cudaGetLastError();
 }

@@ -787,71 +787,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// out[b, h, :] = sum over the pieces of sequence b of 2^(lse_j - lse) O_j.
-__global__ void __launch_bounds__(128) mla_combine_kernel(DecodeArgs a) {
-  __shared__ float w_s[256];
-  __shared__ float stat[2];
-  __shared__ long long pre[2];
-  const int b = blockIdx.x / a.n_h, h = blockIdx.x % a.n_h;
+// out[b, h, :] = sum over the pieces of sequence b of 2^(lse_j - lse) O_j.  One warp
+// per (b, h), no block-wide step: the lanes find the pairs that hold sequence b's keys,
+// reduce the pieces' maximum and weight sum by shuffles, and each lane accumulates 16 of
+// the 512 dims with 16-byte loads of the partials.
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (bh >= a.B * a.n_h) return;  // whole warps only
+  const int b = bh / a.n_h, h = bh % a.n_h;
   const int P = a.n_split;  // pairs
-  if (threadIdx.x < 32) {
-    long long before = 0, total = 0;
-    for (int i = threadIdx.x; i < a.B; i += 32) {
-      const long long L = min(max(a.seqlens[i], 1), a.max_len);
-      total += L;
-      if (i < b) before += L;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-      total += __shfl_xor_sync(0xffffffffu, total, o);
-    }
-    if (threadIdx.x == 0) {
-      pre[0] = before;
-      pre[1] = total;
-    }
+  long long before = 0, total = 0;
+  for (int i = lane; i < a.B; i += 32) {
+    const long long L = min(max(a.seqlens[i], 1), a.max_len);
+    total += L;
+    if (i < b) before += L;
   }
-  __syncthreads();
-  const long long x0 = pre[0], T = pre[1];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  const long long x0 = before, T = total;
   const long long x1 = x0 + min(max(a.seqlens[b], 1), a.max_len) - 1;  // last key of sequence b
   // pair holding key x: the largest p with floor(p T / P) <= x
   const int p_lo = static_cast<int>(((x0 + 1) * P - 1) / T);
   const int p_hi = static_cast<int>(((x1 + 1) * P - 1) / T);
   const int np = p_hi - p_lo + 1;
-  if (threadIdx.x < 32) {
-    // a pair whose key range is empty (fewer keys than pairs) wrote nothing
-    float M = -INFINITY;
-    for (int j = threadIdx.x; j < np; j += 32)
-      if (pair_start(p_lo + j + 1, T, P) > pair_start(p_lo + j, T, P))
-        M = fmaxf(M, a.ws_lse[(static_cast<long long>(p_lo + j) + b) * a.n_h + h]);
+  auto piece_lse = [&](int j) {  // -inf for a pair whose key range is empty (it wrote nothing)
+    if (pair_start(p_lo + j + 1, T, P) <= pair_start(p_lo + j, T, P)) return -INFINITY;
+    return a.ws_lse[(static_cast<long long>(p_lo + j) + b) * a.n_h + h];
+  };
+  float M = -INFINITY;
+  for (int j = lane; j < np; j += 32) M = fmaxf(M, piece_lse(j));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    for (int j = threadIdx.x; j < np; j += 32) {
-      float wgt = 0.f;
-      if (pair_start(p_lo + j + 1, T, P) > pair_start(p_lo + j, T, P))
-        wgt = exp2f(a.ws_lse[(static_cast<long long>(p_lo + j) + b) * a.n_h + h] - M);
-      w_s[j] = wgt;
-      den += wgt;
-    }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float den = 0.f;
+  float4 acc[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (threadIdx.x == 0) {
-      stat[0] = M;
-      stat[1] = den;
+  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < np; j0 += 32) {
+    const float l = j0 + lane < np ? piece_lse(j0 + lane) : -INFINITY;
+    const float wl = l == -INFINITY ? 0.f : exp2f(l - M);
+    den += wl;
+    const int nj = min(32, np - j0);
+    for (int jj = 0; jj < nj; ++jj) {
+      const float w = __shfl_sync(0xffffffffu, wl, jj);
+      if (w == 0.f) continue;  // uniform across the warp
+      const float4* o = reinterpret_cast<const float4*>(
+          a.ws_o + ((static_cast<long long>(p_lo + j0 + jj) + b) * a.n_h + h) * DV);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 v = o[c * 32 + lane];
+        acc[c].x = fmaf(w, v.x, acc[c].x);
+        acc[c].y = fmaf(w, v.y, acc[c].y);
+        acc[c].z = fmaf(w, v.z, acc[c].z);
+        acc[c].w = fmaf(w, v.w, acc[c].w);
+      }
     }
   }
-  __syncthreads();
-  const float inv = 1.f / stat[1];
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<long long>(b) * a.n_h + h) * DV;
-  for (int d = threadIdx.x; d < DV; d += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < np; ++j)
-      if (w_s[j] != 0.f) acc = fmaf(w_s[j], a.ws_o[((static_cast<long long>(p_lo + j) + b) * a.n_h + h) * DV + d], acc);
-    out[d] = __float2bfloat16_rn(acc * inv);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = 1.f / den;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<long long>(bh) * DV;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c].x * inv, acc[c].y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c].z * inv, acc[c].w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + (c * 32 + lane) * 4) = u;
   }
-  if (a.lse != nullptr && threadIdx.x == 0)
-    a.lse[static_cast<long long>(b) * a.n_h + h] = (stat[0] + log2f(stat[1])) * 0.69314718055994530942f;
+  if (a.lse != nullptr && lane == 0) a.lse[bh] = (M + log2f(den)) * 0.69314718055994530942f;
 }
 
 }  // namespace
@@ -927,7 +937,7 @@ cudaError_t launch_decode_mla(const DecodeArgs& a, const RopeFreq& rope, const C
   e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, a, rope, maps[0], maps[1]);
   *launches += 1;
   if (e != cudaSuccess) return e;
-  mla_combine_kernel<<<a.B * a.n_h, 128, 0, st>>>(a);
+  mla_combine_kernel<<<(a.B * a.n_h + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, st>>>(a);
   *launches += 1;
   return cudaGetLastError();
 }

@@ -87,6 +87,7 @@ struct KvAppendArgs {
   long long v_token_stride;
   const int* start;   // device [B]: slot of the first new token of each sequence
   int B, C, n_kv, D_qk, D_v, max_len, rope_offset;
+  int head_groups;    // set by the launcher: threads per (token, 8-dim chunk), each owning n_kv / head_groups heads
 };
 
 // Each launcher returns the launch error (cudaSuccess when enqueued) and adds

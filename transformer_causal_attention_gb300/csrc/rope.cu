@@ -100,14 +100,22 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq f) {
 // rotated at its absolute position start[b] + c and written to that cache
 // slot for every KV head, the value row is copied next to it.
 template <typename T>
+//
+// A decode step appends one token per sequence: too few (token, chunk) items to keep
+// the GPU's loads in flight when each thread walks all heads one after another, so the
+// launcher then gives every head its own thread (head_groups = n_kv; each thread computes
+// its own sin/cos), and otherwise one thread per (token, chunk) for all heads.
 __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq f) {
   const int kch = a.D_qk / 8, vch = a.v_new ? a.D_v / 8 : 0;
   const int per_tok = kch + vch;
-  const long long total = static_cast<long long>(a.B) * a.C * per_tok;
+  const int hg = a.head_groups, hpt = a.n_kv / hg;  // heads per thread
+  const long long total = static_cast<long long>(a.B) * a.C * per_tok * hg;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int ch = static_cast<int>(idx % per_tok);
-    const long long bc = idx / per_tok;
+    const long long r = idx / per_tok;
+    const int h0 = static_cast<int>(r % hg) * hpt;
+    const long long bc = r / hg;
     const int c = static_cast<int>(bc % a.C);
     const int b = static_cast<int>(bc / a.C);
     const int pos = a.start[b] + c;
@@ -116,13 +124,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
     if (ch < kch) {
       const int d0 = ch * 8;
       const int rel = d0 - a.rope_offset;
-      const T* src = static_cast<const T*>(a.k_new) + (bc * a.n_kv) * a.D_qk + d0;
-      T* dst = static_cast<T*>(a.kcache) + slot * a.n_kv * a.D_qk + d0;
+      const T* src = static_cast<const T*>(a.k_new) + (bc * a.n_kv + h0) * a.D_qk + d0;
+      T* dst = static_cast<T*>(a.kcache) + (slot * a.n_kv + h0) * a.D_qk + d0;
       if (rel >= 0 && rel < 2 * f.n_pairs) {
         if (f.half && rel >= f.n_pairs) continue;  // written with its partner chunk
-        rotate_chunk_rows<T, 8>(src, dst, a.D_qk, a.n_kv, rel, pos, f);
+        rotate_chunk_rows<T, 8>(src, dst, a.D_qk, hpt, rel, pos, f);
       } else {
-        for (int h = 0; h < a.n_kv; ++h) {
+        for (int h = 0; h < hpt; ++h) {
           float x[8];
           load_chunk<T, 8>(src + h * a.D_qk, x);
           store_chunk<T, 8>(dst + h * a.D_qk, x);
@@ -130,16 +138,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
       }
     } else {
       const int d0 = (ch - kch) * 8;
-      const T* src = static_cast<const T*>(a.v_new) + (bc * a.n_kv) * a.D_v + d0;
-      T* dst = static_cast<T*>(a.vcache) + slot * a.v_token_stride + d0;
+      const T* src = static_cast<const T*>(a.v_new) + (bc * a.n_kv + h0) * a.D_v + d0;
+      T* dst = static_cast<T*>(a.vcache) + slot * a.v_token_stride + h0 * a.D_v + d0;
       if (a.v_token_stride % 8 == 0) {  // every value chunk starts on a 16-byte boundary: copy whole chunks
-        for (int h = 0; h < a.n_kv; ++h) {
+        for (int h = 0; h < hpt; ++h) {
           float x[8];
           load_chunk<T, 8>(src + h * a.D_v, x);
           store_chunk<T, 8>(dst + h * a.D_v, x);
         }
       } else {
-        for (int h = 0; h < a.n_kv; ++h)
+        for (int h = 0; h < hpt; ++h)
 #pragma unroll
           for (int e = 0; e < 8; ++e) dst[h * a.D_v + e] = src[h * a.D_v + e];
       }
@@ -149,9 +157,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
 
 }  // namespace
 
-cudaError_t launch_kv_append(const KvAppendArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches) {
+cudaError_t launch_kv_append(const KvAppendArgs& args, const RopeFreq& rope, bool bf16, cudaStream_t st,
+                             int* launches) {
+  KvAppendArgs a = args;
   const int per_tok = a.D_qk / 8 + (a.v_new ? a.D_v / 8 : 0);
-  const long long total = static_cast<long long>(a.B) * a.C * per_tok;
+  const long long items = static_cast<long long>(a.B) * a.C * per_tok;
+  // fewer (token, chunk) items than two waves of resident threads (152 SMs x 2048):
+  // one thread per head as well
+  a.head_groups = items < 2LL * 152 * 2048 ? a.n_kv : 1;
+  const long long total = items * a.head_groups;
   long long blocks = (total + 255) / 256;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
