@@ -46,6 +46,20 @@ __device__ __forceinline__ void rope_sincos(int pos, float f_hi, float f_lo, flo
   sincospif(2.0f * t, s, c);
 }
 
+// The same angle, reduced the same way, but its sin/cos taken by the hardware
+// approximations (__sincosf on 2*pi*t, |2*pi*t| <= pi, where CUDA documents an
+// absolute error of about 2^-21.4): a few instructions instead of a polynomial
+// pair.  Used where the rotated value is rounded to bf16 right after (relative
+// step 2^-9), so the difference cannot show; the query rows rotated inside the
+// prefill kernel, whose rotation sits between two work items on the MMA chain.
+__device__ __forceinline__ void rope_sincos_fast(int pos, float f_hi, float f_lo, float* s, float* c) {
+  const float p = static_cast<float>(pos);
+  const float a = p * f_hi;
+  const float e = fmaf(p, f_hi, -a);
+  const float t = (a - rintf(a)) + fmaf(p, f_lo, e);
+  __sincosf(6.28318530717958647692f * t, s, c);
+}
+
 // Rotate the pair (x0, x1) = (x_{2i}, x_{2i+1}) by the angle with sin s, cos c.
 __device__ __forceinline__ void rotate_pair(float& x0, float& x1, float s, float c) {
   const float r0 = x0 * c - x1 * s;
