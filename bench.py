@@ -448,7 +448,9 @@ def run_extras(args):
     workload against its roofline.  L2 is flushed (a 256 MB write) before every
     timed call, outside the events."""
     import torch
-    dev = torch.device("cuda", 0)
+    if int(os.environ.get("RANK", "0")) != 0:  # one GPU's figures; under torchrun rank 0 alone runs
+        return 0
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()

@@ -1,5 +1,6 @@
 """The multi-rank logic of bench.py on CPU: two gloo ranks (as torchrun would start them) agree on the
-maximum of their timings, pass the barrier, and only rank 0 runs and prints the reference arm."""
+maximum of their timings, pass the barrier, and only rank 0 runs and prints the reference arm and the
+--extras line."""
 import os
 import socket
 
@@ -23,8 +24,9 @@ def _rank_main(rank: int, world: int, port: int, out):
     try:
         bench.barrier(world)
         out[rank] = bench.max_over_ranks(1.5 + rank, world)
-        if rank != 0:  # the reference arm: every rank but 0 exits at once, without work or output
+        if rank != 0:  # the reference arm and --extras: every rank but 0 exits at once, without work or output
             out[world + rank] = float(bench.run_reference(type("A", (), {"steps": 1, "warmup": 0})()))
+            out[2 * world + rank] = float(bench.run_extras(type("A", (), {"steps": 1, "warmup": 3, "rows": ""})()))
         bench.barrier(world)
     finally:
         dist.destroy_process_group()
@@ -37,3 +39,4 @@ def test_two_gloo_ranks_take_the_max_and_gate_the_reference_arm():
     mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn", join=True)
     assert out[0] == pytest.approx(2.5) and out[1] == pytest.approx(2.5)
     assert out[world + 1] == 0.0
+    assert out[2 * world + 1] == 0.0
