@@ -75,8 +75,11 @@ struct Cfg {
   static constexpr int kBlockBytes = BM * 128;    // one column block of a tile
   static constexpr int kKStages = DQK == 64 ? 3 : 2;
   static constexpr int kVStages = DQK == 64 ? 3 : (DQK == 128 ? 2 : 1);
+  // Q tile slots: a third slot (D_qk = 64 and 128, where it fits) lets the next
+  // item's first Q tile load while the current item still runs
+  static constexpr int kQSlots = DQK == 192 ? 2 : 3;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kQKTileBytes;
+  static constexpr int kKOff = kQOff + kQSlots * kQKTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kQKTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kVTileBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
@@ -88,7 +91,7 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t q_full[2], q_ready[2], q_empty[2];
+  uint64_t q_full[3], q_ready[3], q_empty[3];  // per Q slot
   uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];  // up to 3 stages
   uint64_t fin;
@@ -262,10 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_items = a.B * a.n_h * n_pairs_q;
 
   if (threadIdx.x == 0) {
+    for (int q = 0; q < C::kQSlots; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->q_ready[q], 128);  // the softmax warpgroup of the tile in the slot
+      mbar_init(&bars->q_empty[q], 128);
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->q_full[t], 1);
-      mbar_init(&bars->q_ready[t], 128);
-      mbar_init(&bars->q_empty[t], 128);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
@@ -298,9 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, a.status, a.wait_limit_ns};
 
-  // Q tile t lives at smem + kQOff + t * kQKTileBytes (arithmetic, not an array:
-  // runtime-indexed local arrays would live in local memory)
-  auto q_smem = [&](int t) { return smem + C::kQOff + t * C::kQKTileBytes; };
+  // Q tile t of this CTA's k-th item lives in slot (2k + t) mod kQSlots, at
+  // smem + kQOff + slot * kQKTileBytes (arithmetic, not an array: runtime-indexed
+  // local arrays would live in local memory); that is the slot's u-th use, u =
+  // (2k + t) / kQSlots, whose barrier phases have parity u & 1.
+  // Each role walks the positions 2k + t in order, keeping (slot, parity) and advancing
+  // them by one or two positions (no division on the hot roles' registers).
+  auto q_smem = [&](uint32_t slot) { return smem + C::kQOff + slot * C::kQKTileBytes; };
+  auto q_advance = [](uint32_t& slot, uint32_t& par, uint32_t by) {  // by <= kQSlots
+    slot += by;
+    if (slot >= static_cast<uint32_t>(C::kQSlots)) {
+      slot -= C::kQSlots;
+      par ^= 1u;
+    }
+  };
 
   if (warp < 4) {
     // control warpgroup: TMA producers (warps 0, 2), the MMA issuer (warp 1)
@@ -322,17 +338,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         uint32_t st = 0, ph = 0;
         uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
-        uint32_t q_issued = 0, it = 0;
+        uint32_t q_armed = 0, q_last = 0, it = 0;  // bit q: slot q loaded / parity of its last load
+        uint32_t qs = 0, qp = 0;                    // slot and parity of position 2 it + t
         for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
           const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           if (is_v) {
-            for (int t = 0; t < 2; ++t) {
-              if (!mbar_wait(&bars->q_empty[t], (it & 1) ^ 1, wc)) goto load_done;
-              mbar_arrive_expect_tx(&bars->q_full[t], C::kQKTileBytes);
+            for (int t = 0; t < 2; ++t, q_advance(qs, qp, 1)) {
+              if (!mbar_wait(&bars->q_empty[qs], qp ^ 1, wc)) goto load_done;
+              mbar_arrive_expect_tx(&bars->q_full[qs], C::kQKTileBytes);
               for (int db = 0; db < C::kQBlocks; ++db)
-                tma_load_4d(q_smem(t) + db * C::kBlockBytes, &tm_q, &bars->q_full[t], db * 64, itm.h,
+                tma_load_4d(q_smem(qs) + db * C::kBlockBytes, &tm_q, &bars->q_full[qs], db * 64, itm.h,
                             (itm.qt0 + t) * BM, itm.b);
-              q_issued = it + 1;
+              q_armed |= 1u << qs;
+              q_last = (q_last & ~(1u << qs)) | (qp << qs);
             }
           }
           for (int v = 0; v < itm.n_load; ++v) {
@@ -351,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bars->abort_flag) {  // let every copy in flight land before shared memory goes away
           for (int s2 = 0; s2 < n_stages; ++s2)
             if (issued & (1u << s2)) drain_wait(&full[s2], (last_ph >> s2) & 1, a.wait_limit_ns);
-          if (q_issued)
-            for (int t = 0; t < 2; ++t) drain_wait(&bars->q_full[t], (q_issued - 1) & 1, a.wait_limit_ns);
+          for (int q = 0; q < C::kQSlots; ++q)
+            if (q_armed & (1u << q)) drain_wait(&bars->q_full[q], (q_last >> q) & 1, a.wait_limit_ns);
         }
       }
       __syncwarp();
@@ -367,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t v_desc0 = sdesc_sw128(smem_u32(smem + C::kVOff), C::kBlockBytes, 1024);
         uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph0 = 0, pph1 = 0;
         uint32_t it = 0;
-        auto issue_qk = [&](int t, uint32_t stage) {
-          const uint64_t a0 = q_desc0 + ((t * C::kQKTileBytes) >> 4);
+        uint32_t qs0 = 0, qp0 = 0;  // slot and parity of Q tile 0 of the current item
+        auto issue_qk = [&](int t, uint32_t qslot, uint32_t stage) {
+          const uint64_t a0 = q_desc0 + ((qslot * C::kQKTileBytes) >> 4);
           const uint64_t b0 = k_desc0 + ((stage * C::kQKTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
@@ -386,15 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
           const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
+          uint32_t qs1 = qs0, qp1 = qp0;
+          q_advance(qs1, qp1, 1);
           if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
           {
             const int j0 = itm.load_at(0);
             for (int t = 0; t < 2; ++t) {
               if (!(t ? itm.r1 : itm.r0).has(j0)) continue;
-              if (!mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+              if (!mbar_wait(&bars->q_ready[t ? qs1 : qs0], t ? qp1 : qp0, wc)) goto mma_done;
               (t ? q_seen1 : q_seen0) = true;
               tc_fence_after();
-              issue_qk(t, kst);
+              issue_qk(t, t ? qs1 : qs0, kst);
               mma_commit(&bars->s_full[t]);
             }
           }
@@ -419,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
                   k_ready = true;
                 }
-                if (!(t ? q_seen1 : q_seen0) && !mbar_wait(&bars->q_ready[t], it & 1, wc)) goto mma_done;
+                if (!(t ? q_seen1 : q_seen0) && !mbar_wait(&bars->q_ready[t ? qs1 : qs0], t ? qp1 : qp0, wc))
+                  goto mma_done;
                 if (t) q_seen1 = true; else q_seen0 = true;
               }
               tc_fence_after();
@@ -433,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
               }
               if (qk) {
-                issue_qk(t, kst);
+                issue_qk(t, t ? qs1 : qs0, kst);
                 mma_commit(&bars->s_full[t]);
               }
             }
@@ -442,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
             }
           }
+          q_advance(qs0, qp0, 2);
         }
       mma_done:
         // every MMA issued so far completes before TMEM is released
@@ -468,20 +491,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1.91 ms).  The MLA shape measured 2% slower that way and keeps the plain order:
     // epilogue, release, then the next item's Q.
     constexpr bool kEarlyQ = DQK != 192;
-    auto prepare_q = [&](uint32_t k, int item_idx) -> bool {
-      if (!warp_wait(&bars->q_full[t], k & 1, wc)) return false;
+    uint32_t cur_qs = static_cast<uint32_t>(t), cur_qp = 0;  // this tile's Q slot and parity in the current item
+    auto prepare_q = [&](uint32_t qs, uint32_t qp, int item_idx) -> bool {
+      if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
       if (f.n_pairs) {
         const Item nx = decode_item<FOLD>(item_idx, a, n_pairs_q, n_kt);
-        rotate_q_row<DQK>(q_smem(t) + r * 128, r, a.q_offset + (nx.qt0 + t) * BM + r, a.rope_offset, f);
+        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t) * BM + r, a.rope_offset, f);
         fence_proxy_async_smem();
       }
-      mbar_arrive(&bars->q_ready[t]);
+      mbar_arrive(&bars->q_ready[qs]);
       return true;
     };
     int idx = item_at<FOLD>(0);
-    if (kEarlyQ && idx < n_items && !prepare_q(0, idx)) idx = n_items;
+    if (kEarlyQ && idx < n_items && !prepare_q(cur_qs, cur_qp, idx)) idx = n_items;
     while (idx < n_items) {
-      if (!kEarlyQ && !prepare_q(it, idx)) break;
+      if (!kEarlyQ && !prepare_q(cur_qs, cur_qp, idx)) break;
       const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
       const TileRange rng = t ? itm.r1 : itm.r0;
@@ -497,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1;
         tc_fence_after();
         // the last Q K of this tile has completed: the producer may load the next item's Q
-        if (kEarlyQ && i == n_t - 1) mbar_arrive(&bars->q_empty[t]);
+        if (kEarlyQ && i == n_t - 1) mbar_arrive(&bars->q_empty[cur_qs]);
         uint32_t sr[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
@@ -589,12 +613,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const int next_idx = item_at<FOLD>(it + 1);
-      if (kEarlyQ && next_idx < n_items && !prepare_q(it + 1, next_idx)) break;
+      uint32_t nxt_qs = cur_qs, nxt_qp = cur_qp;
+      q_advance(nxt_qs, nxt_qp, 2);
+      if (kEarlyQ && next_idx < n_items && !prepare_q(nxt_qs, nxt_qp, next_idx)) break;
 
       // epilogue: O / l -> out (rows past S are computed but not stored)
       if (!warp_wait(&bars->o_done[t], it & 1, wc)) break;
       tc_fence_after();
-      if (!kEarlyQ) mbar_arrive(&bars->q_empty[t]);  // every MMA reading Q_t has completed
+      if (!kEarlyQ) mbar_arrive(&bars->q_empty[cur_qs]);  // every MMA reading Q_t has completed
       const float inv_l = 1.f / l_run;
       const bool store = m < a.S;
       __nv_bfloat16* orow_g = static_cast<__nv_bfloat16*>(a.out) +
@@ -621,6 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.lse[(static_cast<long long>(itm.b) * a.n_h + itm.h) * a.S + m] =
             (m_run + log2f(l_run)) * 0.69314718055994530942f;
       idx = next_idx;
+      cur_qs = nxt_qs;
+      cur_qp = nxt_qp;
       ++it;
     }
   }
