@@ -49,7 +49,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # DRAM bytes (read + write) per launch of the prefill kernel, from the ncu
 # capture summarised in profiles/prefill_tc_llama3_8b.md, valid only for the
 # kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits).
-PREFILL_TRAFFIC = {"kernel_sha": "2f6561705f5ab1fb", "bytes": 4 * 127.955e6}
+PREFILL_TRAFFIC = {"kernel_sha": "1418b8964075f557", "bytes": 4 * 127.557e6}
 
 
 def kernel_sha(name: str) -> str:
