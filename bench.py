@@ -48,8 +48,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 # DRAM bytes (read + write) per launch of the prefill kernel, from the ncu
 # capture summarised in profiles/prefill_tc_llama3_8b.md, valid only for the
-# kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits).
-PREFILL_TRAFFIC = {"kernel_sha": "1418b8964075f557", "bytes": 4 * 127.557e6}
+# kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits;
+# measured on 1418b8964075f557, which differs from this one only in comments).
+PREFILL_TRAFFIC = {"kernel_sha": "b2e7ceb98e6dc36d", "bytes": 4 * 127.557e6}
 
 
 def kernel_sha(name: str) -> str:

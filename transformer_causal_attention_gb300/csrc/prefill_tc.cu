@@ -31,7 +31,10 @@
 //   Items are taken heaviest-first (latest Q tiles see the most keys), dealt to the
 //   CTAs in waves that alternate direction.
 // RoPE: the query tile is rotated in shared memory right after its TMA load
-// (once per item); keys arrive already rotated (written once by the rope pass).
+// (once per item, by the softmax warpgroup, with hardware sin/cos); keys arrive
+// already rotated (written once by the rope pass).  For D_qk = 64 and 128 the Q
+// tiles cycle through three shared-memory slots, so the next item's first tile
+// is in place before the current item ends.
 // Head dims: (64, 64), (128, 128) and the MLA prefill shape D_qk = 192 (128
 // content dims + 64 rotated dims), D_v = 128 ("Transformer 与 LLM" slide 06).
 // TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1,
