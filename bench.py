@@ -444,6 +444,11 @@ def visible_pairs(q_pos, n_keys, window=None, n_sink=0):
     return float(total)
 
 
+def window_decode_keys(L: int, window: int, n_sink: int) -> int:
+    """Keys a decode query at position L - 1 sees: L - 1 - n < window, or n < n_sink."""
+    return min(L, window) + min(n_sink, max(0, L - window))
+
+
 def run_extras(args):
     """One JSON line timing the calls outside the default step, each on its own
     workload against its roofline.  L2 is flushed (a 256 MB write) before every
@@ -550,7 +555,7 @@ def run_extras(args):
         ms = timed(lambda: attn.decode_window(gq, gkc, gvc, gsl, window=win, n_sink=sinks,
                                               rope_base=gc["rope_base"], rope_dims=gc["rope_dims"],
                                               scale=gc["scale"], out=gout, workspace=gws, stream=stream))
-        keys = sum(min(L, win) + min(sinks, max(0, L - win)) for L in gsl_h.tolist())
+        keys = sum(window_decode_keys(L, win, sinks) for L in gsl_h.tolist())
         return hbm_row(f"GQA decode 59 seqs L~U[4096,8192], window {win} + {sinks} sinks", ms,
                        keys * gc["n_kv"] * (gc["D_qk"] + gc["D_v"]) * 2.0)
 
