@@ -151,6 +151,21 @@ ATTN_API int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads,
               attn_dtype_t dtype, void* stream);
 
 /*
+ * attn_rope_at - attn_rope with a position per row instead of consecutive ones:
+ * row s of sequence b is rotated at positions[b * S + s].  Each cached key
+ * carries its own absolute position ("Transformer架构完全深度解析" §7), so rows
+ * whose slots are not consecutive - a batch of requests at different depths,
+ * tokens scattered in a cache - are rotated in one call.
+ *
+ *   positions  DEVICE int32 [B, S] (required, 4-byte aligned); any value is
+ *              rotated as given (positions are meant to be in [0, 2^24), where
+ *              the angle keeps full fp32 accuracy).
+ * Everything else, layouts and errors as attn_rope.
+ */
+ATTN_API int attn_rope_at(void* x_out, const void* x_in, const int* positions, int B, int S, int n_heads, int D,
+                          int rope_offset, int rope_dims, float rope_base, attn_dtype_t dtype, void* stream);
+
+/*
  * attn_prefill_window - attn_prefill with a causal sliding window and
  * attention sinks ("Transformer 与 LLM" slide 07: a window of W keys turns the
  * O(s) KV and compute of each query into O(W); keeping the first few tokens -
@@ -271,8 +286,10 @@ ATTN_API int attn_decode_window(const void* q, const void* kcache, const void* v
  * attn_decode's workspace, so this variant keeps the split-KV partial results
  * in a scratch array compiled into the library instead:
  *  - the array is ATTN_DECODE_STATIC_SCRATCH_BYTES (16 MiB) of device memory
- *    that every GPU holds from the moment the library is loaded on it until
- *    the process exits, whether or not this function is ever called;
+ *    that every GPU holds from the library's first use there (the module is
+ *    loaded lazily by default; with CUDA_MODULE_LOADING=EAGER, from the moment
+ *    the library is loaded) until the process exits, whether or not this
+ *    function is ever called;
  *  - a problem whose attn_decode_workspace_size(...) exceeds that size is
  *    rejected with ATTN_ERR_WORKSPACE before anything is launched (for
  *    example the GQA decode of 59 sequences x 8192 keys, n_h = 32, n_kv = 8,

@@ -35,7 +35,7 @@ def declared_symbols():
 def test_header_and_binding_agree():
     names = set(declared_symbols())
     assert names == {n for n, _, _ in B.SIGNATURES}
-    assert len(names) == 15
+    assert len(names) == 16
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -115,6 +115,14 @@ def test_rope_argument_errors(lib):
     assert r(FAKE, FAKE + 32, 1, 4, 2, 64, 0, 64, 1e4, 0, 1, None) == -1  # partial overlap
     assert r(MISALIGNED, FAKE, 1, 4, 2, 64, 0, 64, 1e4, 0, 1, None) == -3
     assert r(FAKE, FAKE, 1, 4, 2, 1024, 0, 1024, 1e4, 0, 1, None) == -2  # more pairs than the table holds
+
+
+def test_rope_at_argument_errors(lib):
+    r = lib.attn_rope_at
+    assert r(FAKE, FAKE, None, 1, 4, 2, 64, 0, 64, 1e4, 1, None) == -1        # positions are required
+    assert r(FAKE, FAKE, FAKE2, 1, 4, 2, 64, 0, 64, 0.0, 1, None) == -1       # base must be > 0
+    assert r(FAKE, FAKE, FAKE2 + 2, 1, 4, 2, 64, 0, 64, 1e4, 1, None) == -3   # positions not 4-byte aligned
+    assert r(MISALIGNED, FAKE, FAKE2, 1, 4, 2, 64, 0, 64, 1e4, 1, None) == -3
 
 
 def test_wait_limit_and_counter(lib):

@@ -1,8 +1,9 @@
 """Prefill parity: the CUDA library (through the C ABI) against the fp64 oracle.
 
 Covers the tiny fp32 configuration, the GPT-2-shaped configuration in full,
-the Llama-3-8B-shaped configuration at full size on sampled rows (in the launch
-configuration the benchmark times), and small cases that span several tiles,
+the Llama-3-8B-shaped configuration at full size on the edge rows of every
+query tile of every (batch, head) slice (in the launch configuration the
+benchmark times), and small cases that span several tiles,
 a ragged tail, S = 1, MQA, non-causal masking, the CUDA-core path for other
 head sizes, the online-softmax rescale branch and causality.
 """
@@ -80,26 +81,37 @@ def test_gpt2_config_full(lib):
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
 
 
-def test_llama_config_sampled_rows(lib):
+def tile_edge_rows(S, tile=128):
+    """First and last row of every 128-row query tile (the rows a work item starts and ends on)."""
+    rows = set()
+    for t0 in range(0, S, tile):
+        rows.update((t0, min(t0 + tile, S) - 1))
+    return sorted(rows)
+
+
+def test_llama_config_every_slice(lib):
+    # the benchmark's launch: B=4 x 32 heads x 32 tile pairs dealt in waves over the persistent CTAs;
+    # every (b, h) slice is checked at the first and last row of each of its Q tiles, so an item
+    # computed for the wrong slice or tile (or not at all) cannot pass
     cfg = workloads.config("llama3_8b")
     q, k, v = workloads.prefill_inputs(cfg, seed=0)
     out, krot, lse = gpu_prefill(lib, cfg, q, k, v)
     out_c, krot_c, lse_c = out.cpu(), krot.cpu(), lse.cpu()
-    rows = [0, 1, 127, 128, 255, 256, 4095, 4096, 8063, 8064, 8190, 8191]
-    rng = np.random.default_rng(0)
-    got, want = [], []
-    for b, h in [(0, 0), (3, 31), (1, 17), (2, 6)]:
-        sel = sorted(set(rows) | set(rng.integers(0, cfg["S"], 6).tolist()))
-        ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, sel, rope_base=cfg["rope_base"],
-                                                     scale=cfg["scale"])
-        got.append(to_np(out_c[b, sel, h]))
-        want.append(ref)
-        assert np.max(np.abs(to_np(lse_c[b, h, sel]) - ref_lse)) <= BF16_MAX_ABS
-    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", "llama sampled rows")
-    # rotated keys (the cache the prefill writes) on sampled rows of every KV head
-    sel = [0, 1, 4095, 8191]
-    ref_k = oracle.rope_rotate(k[2, sel], np.array(sel)[:, None], cfg["rope_base"])
-    assert_parity(krot_c[2, sel], ref_k, "bf16", "llama k_rot")
+    del out, krot, lse
+    rows = tile_edge_rows(cfg["S"])
+    got, want, worst_lse = [], [], 0.0
+    for b in range(cfg["B"]):
+        for h in range(cfg["n_h"]):
+            ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, rows, rope_base=cfg["rope_base"],
+                                                         scale=cfg["scale"])
+            got.append(to_np(out_c[b, rows, h]))
+            want.append(ref)
+            worst_lse = max(worst_lse, float(np.max(np.abs(to_np(lse_c[b, h, rows]) - ref_lse))))
+    assert worst_lse <= BF16_MAX_ABS, f"lse max-abs {worst_lse}"
+    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", "llama every slice")
+    # the whole rotated-key tensor the prefill writes (the cache a decode reads)
+    for b in range(cfg["B"]):
+        assert_parity(krot_c[b], oracle.rope_cache(k[b:b + 1], cfg["rope_base"])[0], "bf16", f"llama k_rot b={b}")
 
 
 def test_online_softmax_rescale_branch(lib):

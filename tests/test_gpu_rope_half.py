@@ -4,7 +4,8 @@
 apply_rope code) where "Transformer架构从Attention到DecoderBlock" §8.3 pairs
 (2i, 2i+1); §8.1 of the latter allows either as long as training and
 inference agree.  Each test runs one entry point with pairing="half" against
-the oracle's half-split rotation: the RoPE pass, the KV-cache append, the
+the oracle's half-split rotation: the RoPE pass (also at per-row positions,
+attn_rope_at, in both pairings), the KV-cache append, the
 tensor-core and CUDA-core prefill, chunked prefill over a half-split cache, and
 the streaming, generic and MLA decode kernels.
 """
@@ -49,6 +50,36 @@ def test_rope_pass_half_split(lib, D, off, dims, dtype, pos0):
     else:
         assert_parity(y, want, "bf16", "rope half")
     assert torch.equal(y[..., :off].cpu(), x[..., :off])  # dims before the span are copied
+
+
+@pytest.mark.parametrize("pairing,D,off,dims,dtype", [
+    ("adjacent", 128, 0, 128, "bf16"),
+    ("half", 128, 0, 128, "bf16"),
+    ("adjacent", 576, 512, 64, "bf16"),  # the MLA layout: only the last 64 latent dims turn
+    ("adjacent", 12, 4, 8, "f32"),
+])
+def test_rope_at_per_row_positions(lib, pairing, D, off, dims, dtype):
+    # every row at its own absolute position (requests at different depths, tokens scattered in a
+    # cache): attn_rope_at against the oracle's rotation at the same positions
+    cfg = dict(B=3, S=29, n_h=4, n_kv=4, D_h=D, dtype=dtype)
+    x, _, _ = workloads.prefill_inputs(cfg, seed=D + dims)
+    g = torch.Generator().manual_seed(11)
+    pos = torch.randint(0, 1 << 20, (cfg["B"], cfg["S"]), generator=g, dtype=torch.int64).to(torch.int32)
+    pos[0, :4] = torch.tensor([0, 1, 8191, (1 << 24) - 1], dtype=torch.int32)
+    y = lib.rope(x.to(DEV), rope_base=5e5, rope_offset=off, rope_dims=dims, positions=pos.to(DEV), pairing=pairing)
+    torch.cuda.synchronize()
+    want = oracle.rope_rotate(x, pos.numpy()[:, :, None], 5e5, offset=off, dims=dims, pairing=pairing)
+    if dtype == "f32":
+        assert np.max(np.abs(to_np(y) - want)) <= 1e-5
+    else:
+        assert_parity(y, want, "bf16", "rope at per-row positions")
+    # in place, and equal to attn_rope where the positions are consecutive
+    xd = x.to(DEV)
+    seq = (7 + torch.arange(cfg["S"], dtype=torch.int32)).repeat(cfg["B"], 1).to(DEV)
+    a = lib.rope(xd, rope_base=5e5, rope_offset=off, rope_dims=dims, pos_offset=7, pairing=pairing)
+    lib.rope(xd, rope_base=5e5, rope_offset=off, rope_dims=dims, positions=seq, out=xd, pairing=pairing)
+    torch.cuda.synchronize()
+    assert torch.equal(a, xd)
 
 
 @pytest.mark.parametrize("B,S,n_h,n_kv,D,dtype", [

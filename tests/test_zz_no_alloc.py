@@ -6,13 +6,14 @@ owns no memory, a latency-critical token loop that cannot take the device-wide
 synchronisation of cudaMalloc/cudaFree, a runtime with a memory budget fixed at
 start-up).  attn_decode_static keeps the split-KV partials in a 16 MiB scratch
 array compiled into the library.  This test calls it through the C ABI twice in
-a row and compares each result with attn_decode's on the same inputs.  The file
-is named so that pytest collects it last.
+a row and compares each result with attn_decode's on the same inputs and with
+the fp64 oracle.  The file is named so that pytest collects it last.
 """
 
 import pytest
 import torch
 
+import oracle
 import workloads
 from tests.tolerances import assert_parity, to_np
 
@@ -48,11 +49,15 @@ def test_static_scratch_decode_matches_workspace_decode(lib, name, overrides):
                         rope_dims=cfg["rope_dims"], scale=cfg["scale"])
     torch.cuda.synchronize()
     ref_np = to_np(ref)
+    want, _ = oracle.attention_decode(q.cpu(), kc.cpu(), vc.cpu(), sl.cpu().numpy(), rope_base=cfg["rope_base"],
+                                      rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"],
+                                      scale=cfg["scale"])
     for _ in range(2):  # the second call reuses the scratch the first one left behind
         out = torch.full_like(ref, float("nan"))
         assert call_static(raw, q, kc, vc, 0, sl, out, cfg) == 0
         torch.cuda.synchronize()
         assert_parity(out, ref_np, "bf16", "attn_decode_static vs attn_decode")
+        assert_parity(out, want, "bf16", "attn_decode_static vs the fp64 oracle")
     assert lib.device_status() == 0
 
 

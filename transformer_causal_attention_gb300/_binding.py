@@ -32,6 +32,7 @@ SIGNATURES = [
     ("attn_prefill_mla", _i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f, _i, _i,
                               _vp]),
     ("attn_rope", _i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    ("attn_rope_at", _i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     ("attn_prefill_chunk", _i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _f, _i, _i, _vp]),
     ("attn_kv_append", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     ("attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i, _i, _i]),
@@ -208,13 +209,22 @@ def prefill_mla(q, k, v, *, rope_base: float = 0.0, rope_offset: int = 0, rope_d
 
 
 def rope(x, *, rope_base: float, rope_offset: int = 0, rope_dims: int | None = None, pos_offset: int = 0,
-         out=None, pairing: str = "adjacent", stream=None):
-    """RoPE of x [B,S,n_heads,D] at positions pos_offset + s via attn_rope (out may be x)."""
+         positions=None, out=None, pairing: str = "adjacent", stream=None):
+    """RoPE of x [B,S,n_heads,D] (out may be x): at positions pos_offset + s via attn_rope, or,
+    given positions (int32 [B,S] on the device), row (b, s) at positions[b, s] via attn_rope_at."""
     _dev(x, "x")
     B, S, H, D = x.shape
     rope_dims = D - rope_offset if rope_dims is None else rope_dims
     if out is None:
         out = torch.empty_like(x)
+    if positions is not None:
+        _dev(positions, "positions")
+        if positions.dtype != torch.int32 or tuple(positions.shape) != (B, S):
+            raise ValueError("positions must be int32 [B, S]")
+        rc = _lib().attn_rope_at(_ptr(out), _ptr(x), _ptr(positions), B, S, H, D, rope_offset, rope_dims,
+                                 float(rope_base), _dtype_code(x, pairing), _stream_ptr(stream))
+        _check(rc, "attn_rope_at")
+        return out
     rc = _lib().attn_rope(_ptr(out), _ptr(x), B, S, H, D, rope_offset, rope_dims, float(rope_base), pos_offset,
                           _dtype_code(x, pairing), _stream_ptr(stream))
     _check(rc, "attn_rope")

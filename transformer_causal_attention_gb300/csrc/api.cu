@@ -185,8 +185,12 @@ const char* attn_strerror(int code) {
   }
 }
 
-int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D, int rope_offset, int rope_dims,
-              float rope_base, int pos_offset, attn_dtype_t dtype, void* stream) {
+}  // extern "C"
+
+namespace attn {
+namespace {
+int rope_impl(void* x_out, const void* x_in, const int* positions, int B, int S, int n_heads, int D, int rope_offset,
+              int rope_dims, float rope_base, int pos_offset, attn_dtype_t dtype, void* stream) {
   if (!x_out || !x_in || B <= 0 || S <= 0 || n_heads <= 0 || D <= 0) return ATTN_ERR_ARG;
   bool bf16 = false, half = false;
   if (!parse_dtype(dtype, &bf16, &half)) return ATTN_ERR_ARG;
@@ -195,14 +199,30 @@ int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D, i
   const int unit = bf16 ? 8 : 2;  // a thread's chunk of dims; with half pairing each half is whole chunks
   if (D % unit || rope_offset % unit || rope_dims % (half ? 2 * unit : unit)) return ATTN_ERR_ARG;
   if (rope_dims / 2 > kMaxRopePairs) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(x_out) || !aligned16(x_in)) return ATTN_ERR_ALIGN;
+  if (!aligned16(x_out) || !aligned16(x_in) || (reinterpret_cast<uintptr_t>(positions) & 3u)) return ATTN_ERR_ALIGN;
   const size_t bytes = static_cast<size_t>(B) * S * n_heads * D * (bf16 ? 2 : 4);
   if (x_out != x_in && overlap(x_out, bytes, x_in, bytes)) return ATTN_ERR_ARG;
-  RopeArgs ra{x_out, x_in, B, S, n_heads, D, rope_offset, rope_dims, pos_offset};
+  RopeArgs ra{x_out, x_in, B, S, n_heads, D, rope_offset, rope_dims, pos_offset, positions};
   int launches = 0;
   const cudaError_t e =
       launch_rope(ra, make_rope(rope_base, rope_dims, half), bf16, static_cast<cudaStream_t>(stream), &launches);
   return finish(e, launches);
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_rope(void* x_out, const void* x_in, int B, int S, int n_heads, int D, int rope_offset, int rope_dims,
+              float rope_base, int pos_offset, attn_dtype_t dtype, void* stream) {
+  return rope_impl(x_out, x_in, nullptr, B, S, n_heads, D, rope_offset, rope_dims, rope_base, pos_offset, dtype,
+                   stream);
+}
+
+int attn_rope_at(void* x_out, const void* x_in, const int* positions, int B, int S, int n_heads, int D,
+                 int rope_offset, int rope_dims, float rope_base, attn_dtype_t dtype, void* stream) {
+  if (!positions) return ATTN_ERR_ARG;
+  return rope_impl(x_out, x_in, positions, B, S, n_heads, D, rope_offset, rope_dims, rope_base, 0, dtype, stream);
 }
 
 namespace attn {
@@ -270,7 +290,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k
   const RopeFreq rf = make_rope(rope_base, rope ? rope_dims : 0, half);
   if (rope) {
     // rotated keys, written once: the form a KV cache stores
-    RopeArgs ra{k_rot, k, B, S, n_kv, D_qk, rope_offset, rope_dims, 0};
+    RopeArgs ra{k_rot, k, B, S, n_kv, D_qk, rope_offset, rope_dims, 0, nullptr};
     e = launch_rope(ra, rf, bf16, st, &launches);
     if (e != cudaSuccess) return finish(e, launches);
   }

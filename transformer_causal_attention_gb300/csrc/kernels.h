@@ -77,6 +77,7 @@ struct RopeArgs {
   void* out;
   const void* in;
   int B, S, n_heads, D, rope_offset, rope_dims, pos_offset;
+  const int* positions;  // nullable device [B * S]: position of each row; null: pos_offset + s
 };
 
 struct KvAppendArgs {

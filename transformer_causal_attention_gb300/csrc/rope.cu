@@ -6,6 +6,12 @@
 // pass that writes rotated keys (the KV-cache form, "Transformer架构完全深度解析"
 // §7) before the prefill kernel reads them.
 //
+// A row sits at position pos_offset + s (s = its index in the sequence), or at
+// positions[b * S + s] when the caller gives a position per row (tokens whose
+// absolute slots are not consecutive, e.g. a batch of requests at different
+// depths, "Transformer架构完全深度解析" §7: each cached key carries its own
+// absolute position).
+//
 // One thread owns a chunk of CH consecutive dims of one token for ALL heads, so
 // the sin/cos of its pairs are computed once and reused n_heads times.  In the
 // split-halves layout the thread owning a chunk of the first half also owns the
@@ -85,7 +91,8 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq f) {
     const long long off = tok * a.n_heads * a.D + d0;
     if (rel >= 0 && rel < a.rope_dims) {
       if (f.half && rel >= f.n_pairs) continue;  // rotated by the owner of its partner chunk
-      rotate_chunk_rows<T, CH>(in + off, out + off, a.D, a.n_heads, rel, a.pos_offset + s, f);
+      const int pos = a.positions ? a.positions[tok] : a.pos_offset + s;
+      rotate_chunk_rows<T, CH>(in + off, out + off, a.D, a.n_heads, rel, pos, f);
     } else if (in != out) {
       for (int h = 0; h < a.n_heads; ++h) {
         float x[CH];
