@@ -8,10 +8,18 @@ in HBM:
   * gqa     - GQA decode, 59 sequences with 4096..8192 cached keys, n_h=32
     n_kv=8 D_h=128 bf16 (attn_decode: split-KV partials + combine);
   * mla     - MLA-absorbed decode, 32 sequences x 32768 keys, 128 heads over
-    one 576-dim latent head, V = its first 512 dims (attn_decode).
-``value`` is the prefill throughput in TFLOP/s (causal FLOPs = half the dense
-4*B*n_h*S^2*D_h); the decode calls report KV GB/s (algorithmic cache bytes) in
-``parts``.  Every input is larger than the 129 MB L2, so no flush is needed.
+    one 576-dim latent head, V = its first 512 dims (attn_decode);
+  * gpt2    - GPT-2-small-shaped causal MHA prefill, B=8 S=1024 n_h=n_kv=12
+    D_h=64 bf16, no RoPE (attn_prefill).
+``value`` is the Llama prefill throughput in TFLOP/s (causal FLOPs = half the
+dense 4*B*n_h*S^2*D_h); the decode calls report KV GB/s (algorithmic cache
+bytes) and the GPT-2 prefill TFLOP/s in ``parts``.  Every input of the first
+three parts is larger than the 129 MB L2; the GPT-2 part's 48 MB is not, so an
+L2 flush (a 256 MB write, outside its events) precedes each of its calls.
+
+``cpu_baseline`` times the fp64 oracle on the host cores on every one of the
+five configurations: the tiny and GPT-2 prefills in full, the Llama prefill on
+sampled blocks of query rows, the decodes on a subset of their sequences.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--extras]
 
@@ -46,11 +54,10 @@ METRIC = "prefill causal-attn TFLOP/s and decode KV GB/s on 1 GB300, % of roofli
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
-# DRAM bytes (read + write) per launch of the prefill kernel, from the ncu
-# capture summarised in profiles/prefill_tc_llama3_8b.md, valid only for the
-# kernel source it was taken on (sha256 of prefill_tc.cu, first 16 hex digits;
-# measured on 1418b8964075f557, which differs from this one only in comments).
-PREFILL_TRAFFIC = {"kernel_sha": "b2e7ceb98e6dc36d", "bytes": 4 * 127.557e6}
+# DRAM bytes (read + write) per launch of the prefill kernel on the benchmark
+# workload, from an ncu capture of one launch; valid only for the kernel source
+# it was taken on (sha256 of prefill_tc.cu, first 16 hex digits), else null.
+PREFILL_TRAFFIC = {"kernel_sha": "b2e7ceb98e6dc36d", "bytes": 4 * 127.557e6, "scaled_from_b1": True}
 
 
 def kernel_sha(name: str) -> str:
@@ -177,7 +184,7 @@ def sample_rows(cfg, i, n_rows=256):
     return b, h, list(range(r0, r0 + n_rows))
 
 
-def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 12.0, max_samples: int = 512):
+def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 8.0, max_samples: int = 512):
     done, secs, flops = 0, 0.0, 0.0
     while done < max_samples and (done == 0 or secs < budget_s):
         b, h, rows = sample_rows(cfg, done)
@@ -191,7 +198,6 @@ def cpu_baseline_prefill(q, k, v, cfg, budget_s: float = 12.0, max_samples: int 
 
 
 def cpu_baseline_decode(q, kc, vc, sl, cfg, n_seq: int):
-    import numpy as np
     import oracle
     idx = list(range(n_seq))
     t0 = time.perf_counter()
@@ -203,11 +209,27 @@ def cpu_baseline_decode(q, kc, vc, sl, cfg, n_seq: int):
             "sample": f"{n_seq} of {cfg['B']} sequences, fp64, {dt:.1f} s"}
 
 
+def cpu_baseline_full_prefill(cfg, min_s: float = 0.5):
+    """The oracle on a whole prefill configuration, repeated until min_s has passed."""
+    import oracle
+    q, k, v = workloads.prefill_inputs(cfg, seed=0)
+    runs, secs = 0, 0.0
+    while runs == 0 or secs < min_s:
+        t0 = time.perf_counter()
+        oracle.attention_prefill(q, k, v, rope_base=cfg["rope_base"], scale=cfg["scale"])
+        secs += time.perf_counter() - t0
+        runs += 1
+    flops = runs * workloads.causal_flops(cfg["B"], cfg["S"], cfg["n_h"], cfg["D_h"])
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"the whole configuration, {runs} run(s), fp64 from {cfg['dtype']} inputs, {secs:.2f} s"}
+
+
 # ------------------------------------------------------------------ reference arm
 # The workload both arms report (the reference arm times the oracle on samples of its prefill).
 WORKLOAD = ("llama3-8b-shaped causal GQA prefill B=4 S=8192 n_h=32 n_kv=8 D_h=128 RoPE 5e5"
             " + GQA decode 59 seqs L~U[4096,8192] n_h=32 n_kv=8 D_h=128"
-            " + MLA-absorbed decode 32 seqs x 32768 keys, 128 heads, 576/512 latent")
+            " + MLA-absorbed decode 32 seqs x 32768 keys, 128 heads, 576/512 latent"
+            " + GPT-2-small-shaped causal MHA prefill B=8 S=1024 n_h=12 D_h=64")
 
 
 def run_reference(args):
@@ -280,8 +302,17 @@ def run_ours(args):
     mws = torch.empty(attn.decode_workspace_size(mc["B"], mc["n_h"], mc["n_kv"], mc["D_qk"], mc["D_v"],
                                                  mc["max_len"]), dtype=torch.uint8, device=dev)
 
+    g2 = workloads.config("gpt2")
+    g2q_h, g2k_h, g2v_h = workloads.prefill_inputs(g2, seed=rank)
+    g2q, g2k, g2v = g2q_h.to(dev), g2k_h.to(dev), g2v_h.to(dev)
+    g2out = torch.empty_like(g2q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2: the GPT-2 inputs are 48 MB
+
     def prefill():
         attn.prefill(q, k, v, rope_base=pc["rope_base"], scale=pc["scale"], out=out, k_rot=k_rot, stream=stream)
+
+    def gpt2():
+        attn.prefill(g2q, g2k, g2v, scale=g2["scale"], out=g2out, stream=stream)
 
     def gqa():
         attn.decode(gq, gkc, gvc, gsl, rope_base=gc["rope_base"], rope_offset=0, rope_dims=gc["rope_dims"],
@@ -291,7 +322,8 @@ def run_ours(args):
         attn.decode(mq, mkc, mvc, msl, rope_base=mc["rope_base"], rope_offset=mc["rope_offset"],
                     rope_dims=mc["rope_dims"], scale=mc["scale"], out=mout, workspace=mws, stream=stream)
 
-    parts = [(n, fn) for n, fn in (("prefill", prefill), ("gqa", gqa), ("mla", mla)) if n in args.parts]
+    parts = [(n, fn) for n, fn in (("prefill", prefill), ("gqa", gqa), ("mla", mla), ("gpt2", gpt2))
+             if n in args.parts]
     for _ in range(args.warmup):
         for _, fn in parts:
             fn()
@@ -309,6 +341,8 @@ def run_ours(args):
     t_start.record(stream)
     for i in range(args.steps):
         for name, fn in parts:
+            if name == "gpt2":
+                flush.zero_()  # its inputs fit in L2: evict them, outside its events
             a, b = ev[name][i]
             a.record(stream)
             fn()
@@ -324,7 +358,7 @@ def run_ours(args):
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     part_ms = {name: max_over_ranks(sum(a.elapsed_time(b) for a, b in ev[name]), world) / args.steps
                for name, _ in parts}
-    for name in ("prefill", "gqa", "mla"):
+    for name in ("prefill", "gqa", "mla", "gpt2"):
         part_ms.setdefault(name, float("nan"))
     pf_flops = workloads.causal_flops(pc["B"], pc["S"], pc["n_h"], pc["D_h"])
     g_bytes = workloads.decode_bytes(gc, gsl_h.tolist())
@@ -333,6 +367,7 @@ def run_ours(args):
     gqa_gbs = world * g_bytes / (part_ms["gqa"] * 1e-3) / 1e9
     mla_gbs = world * m_bytes / (part_ms["mla"] * 1e-3) / 1e9
     mla_tflops = world * workloads.decode_flops(mc, msl_h.tolist()) / (part_ms["mla"] * 1e-3) / 1e12
+    gpt2_tflops = world * workloads.causal_flops(g2["B"], g2["S"], g2["n_h"], g2["D_h"]) / (part_ms["gpt2"] * 1e-3) / 1e12
 
     hbm_peak = float(peaks["hbm_gbs"])
     bf16_peak = float(peaks["bf16_tflops"])
@@ -342,6 +377,8 @@ def run_ours(args):
                 "frac": per_gpu_prefill / bf16_peak, "traffic": traffic,
                 "kernel": "attn_prefill (RoPE-K pass + prefill_tc_kernel<128>)",
                 "peak_source": f"{peak_kind} bf16 burst"}
+    if traffic is not None and PREFILL_TRAFFIC.get("scaled_from_b1"):
+        roofline["traffic_note"] = "B=1 capture scaled by 4 (L2 held part of a B=1 launch's bytes)"
 
     # ---- end to end through the public API: pinned host inputs in, result out, every step.
     # The batch is pipelined per sequence over three streams: the copy-in of
@@ -394,7 +431,13 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(q_h, k_h, v_h, pc)
-        cpu["decode_gqa"] = cpu_baseline_decode(gq_h, gkc_h, gvc_h, gsl_h, gc, n_seq=4)
+        cpu["configs"] = {
+            "tiny": cpu_baseline_full_prefill(workloads.config("tiny")),
+            "gpt2": cpu_baseline_full_prefill(g2, min_s=0.0),
+            "llama3_8b": {key: cpu[key] for key in ("value", "unit", "cores", "kind", "sample")},
+            "gqa_decode": cpu_baseline_decode(gq_h, gkc_h, gvc_h, gsl_h, gc, n_seq=min(16, gc["B"])),
+            "mla_decode": cpu_baseline_decode(mq_h, mkc_h, mkc_h[..., :mc["D_v"]], msl_h, mc, n_seq=min(8, mc["B"])),
+        }
 
     if rank == 0:
         line = {
@@ -403,7 +446,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD,
-                       "l2": "every input larger than L2 (129 MB); no flush",
+                       "l2": "prefill, GQA and MLA decode inputs larger than L2 (129 MB), no flush; "
+                             "the GPT-2 part: a 256 MB flush write before each call, outside its events",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "parts": {
                 "prefill": {"ms": part_ms["prefill"], "value": prefill_tflops, "unit": "TFLOP/s",
@@ -414,6 +458,10 @@ def run_ours(args):
                 "mla_decode": {"ms": part_ms["mla"], "value": mla_gbs, "unit": "GB/s", "tflops": mla_tflops,
                                "roofline": {"bound": "hbm", "achieved": mla_gbs / world, "peak": hbm_peak,
                                             "unit": "GB/s", "frac": mla_gbs / world / hbm_peak}},
+                "gpt2": {"ms": part_ms["gpt2"], "value": gpt2_tflops, "unit": "TFLOP/s",
+                         "roofline": {"bound": "tensor", "achieved": gpt2_tflops / world, "peak": bf16_peak,
+                                      "unit": "TFLOP/s", "frac": gpt2_tflops / world / bf16_peak},
+                         "l2": "256 MB flush write before each call, outside its events"},
             },
             "roofline": roofline,
             "e2e": e2e,
@@ -641,8 +689,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
-    ap.add_argument("--parts", default="prefill,gqa,mla",
-                    help="comma-separated subset of prefill,gqa,mla (profiling runs)")
+    ap.add_argument("--parts", default="prefill,gqa,mla,gpt2",
+                    help="comma-separated subset of prefill,gqa,mla,gpt2 (profiling runs)")
     ap.add_argument("--extras", action="store_true",
                     help="time the calls outside the default step instead (separate JSON line)")
     ap.add_argument("--rows", default="",
