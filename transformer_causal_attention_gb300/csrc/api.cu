@@ -495,7 +495,7 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, int v_tok
   if (use_mla) {
     CUtensorMap maps[2];
     const unsigned long long row = static_cast<unsigned long long>(D_qk) * 2;
-    if (!make_map3(&maps[0], q, D_qk, n_h, B, row, row * n_h, 128) ||
+    if (!make_map3(&maps[0], q, D_qk, n_h, B, row, row * n_h, 64) ||
         !make_map3(&maps[1], kcache, D_qk, max_len, B, row, row * max_len, kMlaTileKeys))
       return finish(cudaErrorInvalidValue, launches);
     e = launch_decode_mla(da, rf, maps, st, &launches);

@@ -1,4 +1,4 @@
-// decode_mla.cu - MLA-absorbed decode on the tensor cores (sm_103a).
+// decode_mla.cu - MLA-absorbed decode on the tensor cores of a CTA pair (sm_103a).
 //
 // "Transformer 与 LLM" slide 06: after W_UK is folded into the query and W_UV
 // into the output, the 128 query heads of a token share one 576-dim latent KV
@@ -7,51 +7,53 @@
 // against 1152 bytes read - about 242 FLOP per byte, at the ridge of the GPU,
 // so both the tensor cores and HBM must run near their peaks.
 //
-// Mapping.  The fp32 output O is 128 heads x 512 dims = all 512 TMEM columns of
-// an SM, so the two CTAs of a cluster share it: CTA r accumulates the value
-// dims [256 r, 256 r + 256).  The pair walks its keys in rounds of 256; in each
-// round CTA r scores its own 128 keys (S = Q C^T, M = 128 heads, N = 128 keys,
-// K = 576: full tensor-core rate and no score is computed twice), turns them
-// into bf16 probabilities P, keeps P in TMEM for its own P V and writes a copy
-// into the other CTA's shared memory (distributed shared memory), so that each
-// CTA then accumulates O_half += P_own V_own,half + P_peer V_peer,half
-// (M = 128 heads, N = 128 dims per MMA, K = 128 keys).
+// Mapping.  The two CTAs of a cluster act as one tensor-core unit
+// (tcgen05.mma.cta_group::2, issued by the even CTA).  The pair walks its keys in
+// rounds of 256; CTA r holds the round's keys [128 r, 128 r + 128) ("its keys").
+//   scores   S^T [256 keys x 128 heads] = C [256 x 576] Q^T: M = keys (each CTA
+//            supplies its own 128 cache rows as A), N = heads split over the pair
+//            (CTA r holds the query rows of heads [64 r, 64 r + 64), 72 KB, as the
+//            B half it supplies).  Each CTA receives S^T of its own keys in TMEM.
+//   values   O^T [512 dims x 128 heads] += V^T [512 x 256 keys] P^T, as two
+//            M = 256 tiles of dims; CTA r supplies (and accumulates) the dims
+//            [256 t + 128 r, 256 t + 128 r + 128) of tile t, reading those dims of
+//            all 256 keys of the round, and the B half P^T of heads [64 r, +64).
+// The value rows of the other CTA's keys come through L2 (the other CTA read them
+// from HBM for its scores moments before), so every cache byte leaves HBM once.
 //
-// Softmax offsets.  Each row's exponent offset is shared by the pair and moves
-// lazily: a round's probabilities use the offset agreed after the previous
-// round, so no round waits for the other CTA before its exponentials.  With the
-// probabilities each CTA sends its offset, its row maxima and row sums; both
-// CTAs then apply the same rule (raise the offset when a row maximum passes it
-// by 2^8) and so stay in step.  A CTA whose scores pass the shared offset by
-// 2^64 (fp32/bf16 range) uses its own row maximum instead, and the receiving
-// side brings the two halves to the larger offset by scaling O or the peer's P
-// down - both factors are at most one.
+// TMEM (512 columns, allocated for the pair): two S^T buffers (the scores of the
+// next round are computed while the softmax reads the current ones) and O^T
+// (256 columns: two tiles of 128 dims x 128 heads).
 //
-// The copy goes out as asynchronous remote stores that count their bytes on the
-// peer's barrier (st.async with complete_tx), so no fence or remote arrive is
-// on the sending side.
+// Softmax.  One thread per (key, half of the heads): it loads 64 scores of its
+// key from TMEM.  All keys of a head share one exponent offset per round, agreed
+// by the pair before any exponential: each CTA ORs a flag "some score passed the
+// offset by 2^8" over its warps and sends it with, only when set, its per-head
+// maxima; both CTAs then raise a head's offset to the pair's maximum when that
+// passed the old offset by 2^8, rescaling O and the running sums (lazily, as in
+// "Transformer架构完全深度解析" §13's online softmax, where the rescale is exact
+// because O and l always share one reference maximum).  The probabilities go to
+// shared memory as bf16 P^T: the half of the heads this CTA supplies stays local,
+// the other half is stored into the other CTA (st.async, counted on its barrier).
+// The running sums stay per thread until the end of a piece.
 //
-// Loads.  Cache rows stream through a 3-stage ring of 32 KB units (128 keys x
-// 128 dims, two 128-byte-swizzled TMA boxes): five units per round for the
-// scores (the 576 dims), then two of the own keys and two of the peer's keys
-// for P V, restricted to this CTA's value dims (the second read of a row hits
-// L2).  No L2 prefetch: requests ahead of the ring (tensor or bulk prefetch
-// through the TMA engine, or plain prefetches from an idle warp) measured
-// slower or equal.  The query's dims [0, 256) live in TMEM (the score MMA's A
-// operand), dims [256, 576) in shared memory.  Rows at or past a sequence's end
-// may hold anything, so a helper warp zeroes them in the value units before
-// their MMA.  The tensor-core work of round j is issued as P V(own, j), the
-// scores of round j + 1, P V(peer, j): the peer's probabilities arrive while the
-// next scores run.
+// Loads.  Each CTA streams its cache rows through a 3-stage ring of 32 KB units
+// (128 keys x 128 dims, two 128-byte-swizzled TMA boxes) plus one 16 KB slot for
+// the 64 rotary dims, in the order the MMAs take them: scores of round j + 1, then
+// the values of round j.  The odd CTA's copies complete on the even CTA's
+// barriers (cp.async.bulk.tensor .cta_group::2), so the issuer sees both halves
+// of a unit with one wait.  Rows at or past a sequence's end may hold anything:
+// value units that reach past it are cleared by a helper warp in each CTA before
+// their MMA.
 //
 // Keys of all sequences, laid end to end, are split evenly over the pairs (a
-// pair's range may cross sequence boundaries), so every pair does the same
-// work; each (pair, sequence) piece writes one normalised partial, merged per
-// sequence by mla_combine_kernel with the log-sum-exp rule of the online
-// softmax ("Transformer架构完全深度解析" §13).
-// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + single-thread
-// MMA issuer, warp 2 key prefix sums, then the value-row fixer, warps 4-11
-// softmax (two warps per 32 heads = TMEM lanes, 64 keys each) and epilogue.
+// pair's range may cross sequence ends); each (pair, sequence) piece writes one
+// normalised partial, merged per sequence by mla_combine_kernel with the
+// log-sum-exp rule of the online softmax ("Transformer架构完全深度解析" §13).
+// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer (even
+// CTA), warp 2 key prefix sums, then the value-row fixer, warp 3 query RoPE and
+// hand-offs to the even CTA, warps 4-11 softmax (four lane quarters x two halves
+// of the heads) and epilogue.
 #include <math.h>
 
 #include <atomic>
@@ -61,64 +63,77 @@
 namespace attn {
 namespace {
 
-constexpr int NH = 128;              // query heads (MMA M)
+constexpr int NH = 128;              // query heads
+constexpr int HH = 64;               // heads whose query rows one CTA supplies
 constexpr int DQK = 576;             // latent + rotary dims
 constexpr int DV = 512;              // value dims
-constexpr int DVH = 256;             // value dims per CTA of a pair
-constexpr int RK = kMlaTileKeys;     // keys per CTA per round (MMA N of the score tile)
+constexpr int RK = kMlaTileKeys;     // keys per CTA per round
 constexpr int kRoundKeys = 2 * RK;
 constexpr int kThreads = 384;
-constexpr int kBlockBytes = RK * 128;        // 128 rows x 64 bf16 dims, 128-byte swizzled
-constexpr int kUnitBytes = 2 * kBlockBytes;  // one ring stage
+constexpr int kBoxBytes = RK * 128;          // 128 rows x 64 bf16 dims, 128-byte swizzled
+constexpr int kUnitBytes = 2 * kBoxBytes;    // one ring stage: 128 keys x 128 dims
 constexpr int kStages = 3;
-constexpr int kQkUnits = 5;                  // dims [0,128) [128,256) [256,384) [384,512) [512,576)
-constexpr int kQTmemDims = kMlaQTmemDims;    // query dims [0, 256) live in TMEM
-constexpr int kQSmemBlocks = (DQK - kQTmemDims) / 64;  // dims [256, 576) in shared memory: 5 blocks
-static_assert(NH == RK, "query blocks and cache blocks share one box shape");
-static_assert(kQTmemDims == 256, "the score units 0 and 1 read the query from TMEM");
-constexpr int kQSmemBytes = kQSmemBlocks * kBlockBytes;  // 80 KB
-constexpr int kMaxB = 256;  // the batch's key prefix sums live in shared memory
+constexpr int kQkUnits = 5;                  // dims [0,128) [128,256) [256,384) [384,512) | [512,576)
+constexpr int kQBlockBytes = HH * 128;       // 64 heads x 64 dims
+constexpr int kQBlocks = DQK / 64;           // 9
+constexpr int kQBytes = kQBlocks * kQBlockBytes;   // 72 KB
+constexpr int kPTBytes = kRoundKeys * 128;   // P^T: 256 keys x 64 heads, bf16
+constexpr int kMaxB = 256;                   // the batch's key prefix sums live in shared memory
+static_assert(RK == 128, "one TMEM lane per key of a CTA");
+
+// shared memory (every MMA operand 1024-byte aligned)
 constexpr int kQOff = 0;
-constexpr int kRingOff = kQOff + kQSmemBytes;
-constexpr int kPPOff = kRingOff + kStages * kUnitBytes;  // the peer's P: 2 blocks (keys 0-63, 64-127)
-constexpr int kMsgOff = kPPOff + 2 * kBlockBytes;        // the peer's offsets, maxima, row sums
-constexpr int kRedOff = kMsgOff + 4 * NH * 4;            // row maxima of the two key halves, 2 rounds; row sums
-constexpr int kPrefOff = kRedOff + 6 * NH * 4;
+constexpr int kRingOff = kQOff + kQBytes;
+constexpr int kRopeOff = kRingOff + kStages * kUnitBytes;  // the slot of the 64 rotary dims
+constexpr int kPTOff = kRopeOff + kBoxBytes;
+constexpr int kMsgWords = NH + 4;                          // per-head maxima, then a flag word
+constexpr int kMsgOff = kPTOff + kPTBytes;                 // [2 round parities] messages from the other CTA
+constexpr int kRedOff = kMsgOff + 2 * kMsgWords * 4;       // [4 lane quarters][128 heads] partial maxima / sums
+constexpr int kMOff = kRedOff + 4 * NH * 4;                // [8 softmax warps][64 heads] offsets, one copy per warp
+constexpr int kFacOff = kMOff + 8 * HH * 4;                // [8 softmax warps][64 heads] rescale factors of a round
+constexpr int kLOff = kFacOff + 8 * HH * 4;                // [2][128]: this CTA's row sums, the other CTA's
+constexpr int kFlagOff = kLOff + 2 * NH * 4;               // [2 round parities][8 warps] exceed flags
+constexpr int kPrefOff = kFlagOff + 64;
 constexpr int kBarOff = kPrefOff + ((kMaxB + 1) * 4 + 63) / 64 * 64;
 constexpr int kUsedBytes = kBarOff + 512;
 constexpr int kSmemBytes = kUsedBytes + 1024;  // + slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-// TMEM columns: S (fp32, 128) whose first halves of each 64-key half take P as bf16 pairs,
-// O_half (256), the query dims [0, 256) as bf16 pairs (128)
-constexpr uint32_t kSCol = 0;
-constexpr uint32_t kOCol = 128;
-constexpr uint32_t kQCol = 384;
-constexpr uint32_t kIdescQK = idesc_bf16_f32(NH, RK, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(NH, 128, true);
-constexpr float kRaise = 8.0f;       // the shared offset moves when a row maximum passes it by 2^8
-constexpr float kEmergency = 64.0f;  // a CTA uses its own maximum when its scores pass the offset by 2^64
-// bytes the peer stores per round: P (128 heads x 128 keys bf16), offsets, maxima, row sums
-constexpr uint32_t kMsgBytes = NH * RK * 2 + 4 * NH * 4;
+static_assert(kRingOff % 1024 == 0 && kRopeOff % 1024 == 0 && kPTOff % 1024 == 0, "operand alignment");
+constexpr uint32_t kMsgBytes = (NH + 1) * 4;   // the maxima and the flag word
+constexpr uint32_t kPTPeerBytes = RK * 128;   // the other CTA's 128 key rows of this CTA's P^T
 
-struct Msg {  // written by the peer CTA each round
-  float m_own[NH];  // offset its P used
-  float mx[NH];     // its row maxima (log2 domain)
-  float rs[2][NH];  // its row sums, per 64-key half
-};
-static_assert(sizeof(Msg) == 4 * NH * 4, "message layout");
+// TMEM columns
+constexpr uint32_t kSCol = 0;     // S^T buffers at 0 and 128
+constexpr uint32_t kOCol = 256;   // O^T tiles at 256 and 384
+constexpr uint32_t kIdescQK = idesc_bf16_f32(256, NH, false);
+// O^T = V^T P^T: A (V^T, dims x keys) and B (P^T, keys x heads) are both contiguous along M / N
+constexpr uint32_t kIdescPV = idesc_bf16_f32(256, NH, true) | (1u << 15);
+constexpr float kRaise = 8.0f;    // a head's offset moves when the pair's maximum passes it by 2^8
+
+// Register split: the launch holds 168 registers per thread (384 threads, one CTA per SM); the
+// control warps drop to kRegsCtl, the softmax warps rise to kRegsSoftmax (64 scores, 64 running
+// sums and the packed probabilities of a thread).  setmaxnreg.inc waits until the pool has the
+// registers, so the split must fit it; the launcher checks the compiled count before launching.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtl = 104, kRegsSoftmax = 200;
+constexpr int kRegsNeeded = 4 * 32 * kRegsCtl + 8 * 32 * kRegsSoftmax;
+static_assert(kRegsNeeded <= kThreads * kLaunchRegs, "register split exceeds the launch's pool");
+constexpr float kNoOffset = -1e30f;
 
 struct Bars {
+  uint64_t kv_full[kStages], kv_fixed[kStages], kv_tofix[kStages], kv_empty[kStages];
+  uint64_t rope_full, rope_empty;
   uint64_t q_full, q_ready, q_empty;
-  uint64_t kv_full[kStages], kv_tofix[kStages], kv_fixed[kStages], kv_empty[kStages];
-  uint64_t s_full, p_ready, pvo_done, pp_full, pp_ready, pvp_done, pp_empty;
-  uint64_t o_empty, fin;
-  uint64_t hsync[4];  // the two softmax warps of 32 heads exchange row maxima / sums (64 arrivals)
+  uint64_t s_full[2], s_free[2];
+  uint64_t hsync[2];   // among the 8 softmax warps of a CTA: [0] the round's flags, [1] maxima / sums
+  uint64_t msg_full[2];
+  uint64_t pt_full, pt_ready;
+  uint64_t pv_done, o_empty, l_full, fin;
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// First key (in the concatenation of all sequences) of pair p.
 __device__ __forceinline__ long long pair_start(int p, long long T, int P) {
   return static_cast<long long>(p) * T / P;
 }
@@ -141,7 +156,6 @@ struct PieceIter {
     }
     b = lo;
   }
-  // next piece: sequence *sb, keys [*lo, *hi) of that sequence
   __device__ bool next(int* sb, int* lo, int* hi) {
     if (x >= end || b >= B) return false;
     const long long seq_end = prefix[b + 1];
@@ -155,78 +169,66 @@ struct PieceIter {
   }
 };
 
-// One unit of a piece's load stream: keys [key0, key0 + 128) of the sequence,
-// 64-dim blocks [blk0, blk0 + nblk).  Value units are read by P V.
+// One unit of the load stream: keys [key0, key0 + 128), 64-dim boxes starting at dim d0 (d0 + 64 for the
+// second box).  Score units carry this CTA's keys; value units carry the keys of one CTA of the pair and
+// this CTA's dims of one O^T tile.
 struct Unit {
-  int key0, blk0, nblk;
+  int key0, d0, nbox;
+  bool rope_slot;  // the 64 rotary dims: its own slot
   bool pv;
 };
 __device__ __forceinline__ Unit qk_unit(int lo, int j, int r, int u) {
-  return Unit{lo + j * kRoundKeys + r * RK, 2 * u, u == kQkUnits - 1 ? 1 : 2, false};
+  return Unit{lo + j * kRoundKeys + r * RK, 128 * u, u == kQkUnits - 1 ? 1 : 2, u == kQkUnits - 1, false};
 }
-__device__ __forceinline__ Unit pv_unit(int lo, int j, int owner, int r, int v) {
-  return Unit{lo + j * kRoundKeys + owner * RK, 4 * r + 2 * v, 2, true};
+__device__ __forceinline__ Unit pv_unit(int lo, int j, int r, int kh, int t) {
+  return Unit{lo + j * kRoundKeys + kh * RK, 256 * t + 128 * r, 2, false, true};
 }
-// A value unit reaching past the sequence (length L) has rows to clear.
 __device__ __forceinline__ bool needs_fix(const Unit& u, int L) { return u.pv && u.key0 + RK > L; }
 
-// Every unit of a piece with nr rounds, in the order the MMA issuer takes them:
-// scores(0), then per round j: P V(own, j), scores(j + 1), P V(peer, j).
+// Every unit of a piece with nr rounds in the order the MMAs take them: scores(0), then for
+// j = 1 .. nr - 1: scores(j), values(j - 1); then values(nr - 1).
 template <typename F>
 __device__ __forceinline__ bool for_units(int lo, int nr, int r, F&& f) {
-  for (int u = 0; u < kQkUnits; ++u)
-    if (!f(qk_unit(lo, 0, r, u), 0)) return false;
-  for (int j = 0; j < nr; ++j) {
-    for (int v = 0; v < 2; ++v)
-      if (!f(pv_unit(lo, j, r, r, v), j)) return false;
-    if (j + 1 < nr)
+  for (int j = 0; j <= nr; ++j) {
+    if (j < nr)
       for (int u = 0; u < kQkUnits; ++u)
-        if (!f(qk_unit(lo, j + 1, r, u), j + 1)) return false;
-    for (int v = 0; v < 2; ++v)
-      if (!f(pv_unit(lo, j, r ^ 1, r, v), j)) return false;
+        if (!f(qk_unit(lo, j, r, u))) return false;
+    if (j >= 1)
+      for (int kh = 0; kh < 2; ++kh)
+        for (int t = 0; t < 2; ++t)
+          if (!f(pv_unit(lo, j - 1, r, kh, t))) return false;
   }
   return true;
 }
 
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            int c2) {
+// ---- pair (cluster) helpers
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+// TMA load whose completion is counted on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
       : "memory");
 }
-
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  const bool ok = mbar_wait(bar, parity, w);
-  return __all_sync(0xffffffffu, ok);
+__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return;
-  }
-}
-
-// ---- cluster (distributed shared memory) helpers
-__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-  return r;
-}
-// Asynchronous stores into the peer CTA's shared memory; each counts its bytes on the
-// peer's barrier (complete_tx), so the peer sees them once its barrier phase completes.
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
-                                           uint32_t bar) {
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                            uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                    addr),
                "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
-               "r"(__float_as_uint(v)), "r"(bar)
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -240,8 +242,8 @@ __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a barrier that the other CTA arrives on (acquire at cluster scope).
-__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+// Bounded wait on a barrier that the other CTA (or its copies) may complete (acquire at cluster scope).
+__device__ __forceinline__ bool wait_cl(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -256,79 +258,113 @@ __device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, con
     }
   }
 }
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  const bool ok = wait_cluster(bar, parity, w);
+__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  const bool ok = wait_cl(bar, parity, w);
   return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!try_wait_cluster(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive once on the barrier at the same offset in the CTAs of mask when every
-// tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+
+// ---- tcgen05 for the pair (every tcgen05 instruction of this kernel uses cta_group::2)
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Arrive once on the barrier at this offset in both CTAs when the pair's MMAs issued so far complete.
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+__device__ __forceinline__ void commit_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 
-// O_half columns [kOCol + 128 kh, + 128) of this thread's row times f.  The TMEM loads and
-// stores are warp-collective: every lane of the warp calls this (f = 1 where nothing moves).
-__device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
+// columns [col, col + 64) of this thread's TMEM lane (taddr) times the per-column factors f[0..63]
+// (shared memory); warp-collective
+__device__ __forceinline__ void scale_cols64(uint32_t taddr, const float* f) {
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t o[32];
     tmem_ld32(taddr + c * 32, o);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+    for (int e = 0; e < 32; e += 4) {
+      const float4 f4 = *reinterpret_cast<const float4*>(f + c * 32 + e);
+      o[e] = __float_as_uint(__uint_as_float(o[e]) * f4.x);
+      o[e + 1] = __float_as_uint(__uint_as_float(o[e + 1]) * f4.y);
+      o[e + 2] = __float_as_uint(__uint_as_float(o[e + 2]) * f4.z);
+      o[e + 3] = __float_as_uint(__uint_as_float(o[e + 3]) * f4.w);
+    }
     tmem_st32(taddr + c * 32, o);
   }
-  tmem_wait_st();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the shared array, so that the compiler keeps shared-memory addressing
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   int* prefix = reinterpret_cast<int*>(smem + kPrefOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = gridDim.x >> 1;           // pairs (clusters of two CTAs)
-  const int p = blockIdx.x >> 1;          // this CTA's pair
-  const int r = blockIdx.x & 1;           // rank in the cluster = value-dim half
+  const int P = gridDim.x >> 1;   // pairs
+  const int p = blockIdx.x >> 1;  // this CTA's pair
+  const int r = blockIdx.x & 1;   // rank in the pair; 0 issues the MMAs
   const bool layout_ok = static_cast<int>(smem - smem_raw) + kUsedBytes <= kSmemBytes;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_ready, 128);
-    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_fixed[s], 2);  // the fixers of both CTAs
       mbar_init(&bars->kv_tofix[s], 1);
-      mbar_init(&bars->kv_fixed[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_ready, 256);
-    mbar_init(&bars->pvo_done, 1);
-    mbar_init(&bars->pp_full, 1);  // armed locally each round with the message's byte count
-    mbar_arrive_expect_tx(&bars->pp_full, kMsgBytes);  // round 0, before the peer can store
-    mbar_init(&bars->pp_ready, 256);
-    mbar_init(&bars->pvp_done, 1);
-    mbar_init(&bars->pp_empty, 1);
-    mbar_init(&bars->o_empty, 256);
+    mbar_init(&bars->rope_full, 1);
+    mbar_init(&bars->rope_empty, 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_ready, 2);   // both CTAs' queries loaded (and rotated)
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 16);  // the 8 softmax warps of both CTAs
+      mbar_init(&bars->hsync[i], 8);
+      mbar_init(&bars->msg_full[i], 1);
+    }
+    mbar_arrive_expect_tx(&bars->msg_full[0], kMsgBytes);  // rounds 0 and 1, before the other CTA can store
+    mbar_arrive_expect_tx(&bars->msg_full[1], kMsgBytes);
+    mbar_init(&bars->pt_full, 8);
+    mbar_init(&bars->pt_ready, 1);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_empty, 16);
+    mbar_init(&bars->l_full, 1);
+    mbar_arrive_expect_tx(&bars->l_full, NH * 4);  // the first piece's row sums
     mbar_init(&bars->fin, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->hsync[i], 64);
     bars->abort_flag = layout_ok ? 0 : 1;
     if (!layout_ok) atomicOr(a.status, STATUS_LAYOUT);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&bars->tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   if (warp == 2) {
     // prefix[b] = number of keys of sequences before b (lengths clamped to [1, max_len])
@@ -348,14 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // both CTAs' barriers are initialised before either arrives remotely
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, a.status, a.wait_limit_ns};
   const long long T = prefix[a.B];
   const long long k_begin = pair_start(p, T, P), k_end = pair_start(p + 1, T, P);
   const bool run = !bars->abort_flag;  // false: the shared-memory layout did not fit, touch nothing
+  const uint32_t peer = static_cast<uint32_t>(r ^ 1);
 
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && run) {
@@ -363,147 +402,138 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_c);
       PieceIter it;
       it.init(prefix, a.B, k_begin, k_end);
-      uint32_t st = 0, ph = 0, q_issued = 0, issued = 0;
-      uint64_t* last_bar[kStages] = {};
-      uint32_t last_par[kStages] = {};
-      uint32_t fullph = 0, fixph = 0;  // bit s: phase of kv_full[s] / kv_tofix[s]
+      uint32_t st = 0, ph = 0, rph = 0, any_issued = 0;
       int sb, lo, hi;
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
         const int L = prefix[sb + 1] - prefix[sb];
         const int nr = (hi - lo + kRoundKeys - 1) / kRoundKeys;
-        if (!mbar_wait(&bars->q_empty, (n & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&bars->q_full, kQSmemBytes);
-        for (int blk = 0; blk < kQSmemBlocks; ++blk)
-          tma_load_3d(smem + kQOff + blk * kBlockBytes, &tm_q, &bars->q_full, kQTmemDims + blk * 64, 0, sb);
-        q_issued = n + 1;
-        const bool done = for_units(lo, nr, r, [&](const Unit& u, int) -> bool {
-          if (!mbar_wait(&bars->kv_empty[st], ph ^ 1, wc)) return false;
-          const bool fix = needs_fix(u, L);
-          uint64_t* bar = fix ? &bars->kv_tofix[st] : &bars->kv_full[st];
-          uint32_t& bits = fix ? fixph : fullph;
-          mbar_arrive_expect_tx(bar, u.nblk * kBlockBytes);
+        if (!wait_cl(&bars->q_empty, (n & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+        for (int blk = 0; blk < kQBlocks; ++blk)
+          tma_load_3d_pair(smem + kQOff + blk * kQBlockBytes, &tm_q, smem_u32(&bars->q_full), blk * 64, HH * r, sb);
+        any_issued = 1;
+        const bool done = for_units(lo, nr, r, [&](const Unit& u) -> bool {
+          if (u.rope_slot) {
+            if (!wait_cl(&bars->rope_empty, rph ^ 1, wc)) return false;
+            if (r == 0) mbar_arrive_expect_tx(&bars->rope_full, 2 * kBoxBytes);
+            tma_load_3d_pair(smem + kRopeOff, &tm_c, cluster_addr(&bars->rope_full, 0), u.d0, u.key0, sb);
+            rph ^= 1;
+            return true;
+          }
+          if (!wait_cl(&bars->kv_empty[st], ph ^ 1, wc)) return false;
           uint8_t* dst = smem + kRingOff + st * kUnitBytes;
-          for (int b = 0; b < u.nblk; ++b) tma_load_3d(dst + b * kBlockBytes, &tm_c, bar, (u.blk0 + b) * 64, u.key0, sb);
-          last_bar[st] = bar;
-          last_par[st] = (bits >> st) & 1u;
-          bits ^= 1u << st;
-          issued |= 1u << st;
+          if (needs_fix(u, L)) {  // counted locally, cleared by this CTA's fixer, then handed on
+            mbar_arrive_expect_tx(&bars->kv_tofix[st], u.nbox * kBoxBytes);
+            const uint32_t bar = cluster_addr(&bars->kv_tofix[st], static_cast<uint32_t>(r));
+            for (int b = 0; b < u.nbox; ++b) tma_load_3d_pair(dst + b * kBoxBytes, &tm_c, bar, u.d0 + 64 * b, u.key0, sb);
+          } else {
+            if (r == 0) mbar_arrive_expect_tx(&bars->kv_full[st], 2 * u.nbox * kBoxBytes);
+            const uint32_t bar = cluster_addr(&bars->kv_full[st], 0);
+            for (int b = 0; b < u.nbox; ++b) tma_load_3d_pair(dst + b * kBoxBytes, &tm_c, bar, u.d0 + 64 * b, u.key0, sb);
+          }
           if (++st == kStages) { st = 0; ph ^= 1; }
           return true;
         });
         if (!done) break;
       }
-      if (bars->abort_flag) {  // let every copy in flight land before the CTA may exit
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) drain_wait(last_bar[s], last_par[s], a.wait_limit_ns);
-        if (q_issued) drain_wait(&bars->q_full, (q_issued - 1) & 1, a.wait_limit_ns);
+      if (bars->abort_flag && any_issued) {
+        // copies in flight may still land: give them time before the CTA can leave (their barriers may sit
+        // in the other CTA, so waiting on them is not always possible here)
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && run) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && run && r == 0) {
       PieceIter it;
       it.init(prefix, a.B, k_begin, k_end);
       const uint32_t q_addr = smem_u32(smem + kQOff);
-      const uint32_t pp_addr = smem_u32(smem + kPPOff);
-      uint32_t st = 0, fullph = 0, fixph = 0, G = 0;
+      const uint32_t pt_addr = smem_u32(smem + kPTOff);
+      uint32_t st = 0, fullph = 0, fixph = 0, rph = 0, g = 0, gp = 0;
       int sb, lo, hi, L = 0;
-      // wait for the unit in the current stage (cleared value units come through the fixer)
       auto take = [&](const Unit& u) -> bool {
-        if (needs_fix(u, L)) {
-          if (!mbar_wait(&bars->kv_fixed[st], (fixph >> st) & 1u, wc)) return false;
+        if (u.rope_slot) {
+          if (!wait_cl(&bars->rope_full, rph, wc)) return false;
+          rph ^= 1;
+        } else if (needs_fix(u, L)) {
+          if (!wait_cl(&bars->kv_fixed[st], (fixph >> st) & 1u, wc)) return false;
           fixph ^= 1u << st;
         } else {
-          if (!mbar_wait(&bars->kv_full[st], (fullph >> st) & 1u, wc)) return false;
+          if (!wait_cl(&bars->kv_full[st], (fullph >> st) & 1u, wc)) return false;
           fullph ^= 1u << st;
         }
         tc_fence_after();
         return true;
       };
-      auto release = [&]() {
-        mma_commit(&bars->kv_empty[st]);
-        if (++st == kStages) st = 0;
-      };
-      // S (+)= Q[:, dims of unit u] C[keys, dims of unit u]^T
-      auto issue_qk = [&](int u) {
-        const uint32_t kaddr = smem_u32(smem + kRingOff + st * kUnitBytes);
-        const int nb = u == kQkUnits - 1 ? 1 : 2;
-        for (int b = 0; b < nb; ++b) {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = 8 * u + 4 * b + k4;  // 16-dim step over the 576 dims
-            const uint64_t bdesc = sdesc_sw128(kaddr + b * kBlockBytes + k4 * 32, 16, 1024);
-            if (kk < kQTmemDims / 16) {
-              mma_ts(tmem + kSCol, tmem + kQCol + kk * 8, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
-            } else {
-              const int kq = kk - kQTmemDims / 16;
-              mma_ss(tmem + kSCol, sdesc_sw128(q_addr + (kq >> 2) * kBlockBytes + (kq & 3) * 32, 16, 1024), bdesc,
-                     kIdescQK, 1u);
-            }
-          }
+      auto release = [&](const Unit& u) {
+        if (u.rope_slot) {
+          commit_both(&bars->rope_empty);
+        } else {
+          commit_both(&bars->kv_empty[st]);
+          if (++st == kStages) st = 0;
         }
       };
-      // O_half[:, 128 v .. 128 v + 128) (+)= P C[keys, value dims]: P from TMEM (own keys) or from
-      // the peer's copy in shared memory
-      auto issue_pv = [&](int v, bool own, bool accumulate) {
-        const uint32_t vaddr = smem_u32(smem + kRingOff + st * kUnitBytes);
-#pragma unroll
-        for (int kk = 0; kk < RK / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vaddr + kk * 16 * 128, kBlockBytes, 1024);
-          const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-          if (own)
-            mma_ts(tmem + kOCol + 128 * v, tmem + kSCol + (kk >> 2) * 64 + (kk & 3) * 8, bdesc, kIdescPV, acc);
-          else
-            mma_ss(tmem + kOCol + 128 * v,
-                   sdesc_sw128(pp_addr + (kk >> 2) * kBlockBytes + (kk & 3) * 32, 16, 1024), bdesc, kIdescPV, acc);
-        }
-      };
-      auto scores = [&](int j) -> bool {
-        for (int u = 0; u < kQkUnits; ++u) {
-          if (!take(qk_unit(lo, j, r, u))) return false;
-          issue_qk(u);
-          release();
-        }
-        mma_commit(&bars->s_full);
-        return true;
-      };
-      const uint16_t peer_mask = static_cast<uint16_t>(1u << (r ^ 1));
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
         L = prefix[sb + 1] - prefix[sb];
         const int nr = (hi - lo + kRoundKeys - 1) / kRoundKeys;
-        if (!mbar_wait(&bars->q_ready, n & 1, wc)) goto mma_done;
+        if (!wait_cl(&bars->q_ready, n & 1, wc)) goto mma_done;
         tc_fence_after();
-        if (!scores(0)) goto mma_done;
-        if (nr == 1) mma_commit(&bars->q_empty);  // every MMA reading this query is issued
-        for (int j = 0; j < nr; ++j, ++G) {
-          if (!mbar_wait(&bars->p_ready, G & 1, wc)) goto mma_done;
-          if (j == 0 && !mbar_wait(&bars->o_empty, (n & 1) ^ 1, wc)) goto mma_done;
-          tc_fence_after();
-          for (int v = 0; v < 2; ++v) {
-            if (!take(pv_unit(lo, j, r, r, v))) goto mma_done;
-            issue_pv(v, true, j > 0);
-            release();
+        for (int j = 0; j <= nr; ++j) {
+          if (j < nr) {
+            // S^T (+)= C Q^T over the 576 dims: 36 MMAs of 16 dims
+            const uint32_t buf = g & 1;
+            if (!wait_cl(&bars->s_free[buf], ((g >> 1) & 1) ^ 1, wc)) goto mma_done;
+            tc_fence_after();
+            for (int u = 0; u < kQkUnits; ++u) {
+              const Unit un = qk_unit(lo, j, 0, u);
+              if (!take(un)) goto mma_done;
+              const uint32_t base = un.rope_slot ? smem_u32(smem + kRopeOff) : smem_u32(smem + kRingOff + st * kUnitBytes);
+              for (int b = 0; b < un.nbox; ++b) {
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                  const int qb = 2 * u + b;  // 64-dim block of the query
+                  mma_pair(tmem + kSCol + 128 * buf, sdesc_sw128(base + b * kBoxBytes + k4 * 32, 16, 1024),
+                           sdesc_sw128(q_addr + qb * kQBlockBytes + k4 * 32, 16, 1024), kIdescQK,
+                           (u | b | k4) ? 1u : 0u);
+                }
+              }
+              release(un);
+            }
+            commit_both(&bars->s_full[buf]);
+            if (j == nr - 1) commit_both(&bars->q_empty);  // every MMA reading this query is issued
+            ++g;
           }
-          mma_commit(&bars->pvo_done);
-          if (j + 1 < nr) {
-            if (!scores(j + 1)) goto mma_done;
-            if (j + 1 == nr - 1) mma_commit(&bars->q_empty);
+          if (j >= 1) {
+            // O^T (+)= V^T P^T over the round's 256 keys, two tiles of 256 dims
+            if (!wait_cl(&bars->pt_full, gp & 1, wc)) goto mma_done;
+            if (!wait_cl(&bars->pt_ready, gp & 1, wc)) goto mma_done;
+            if (j == 1 && !wait_cl(&bars->o_empty, (n & 1) ^ 1, wc)) goto mma_done;
+            tc_fence_after();
+            fence_proxy_async_smem();
+            for (int kh = 0; kh < 2; ++kh) {
+              for (int t = 0; t < 2; ++t) {
+                const Unit un = pv_unit(lo, j - 1, 0, kh, t);
+                if (!take(un)) goto mma_done;
+                const uint32_t vaddr = smem_u32(smem + kRingOff + st * kUnitBytes);
+#pragma unroll
+                for (int i = 0; i < RK / 16; ++i) {
+                  mma_pair(tmem + kOCol + 128 * t, sdesc_sw128(vaddr + i * 16 * 128, kBoxBytes, 1024),
+                           sdesc_sw128(pt_addr + (kh * RK + i * 16) * 128, kBoxBytes, 1024), kIdescPV,
+                           (j > 1 || kh > 0 || i > 0) ? 1u : 0u);
+                }
+                release(un);
+              }
+            }
+            commit_both(&bars->pv_done);
+            ++gp;
           }
-          if (!mbar_wait(&bars->pp_ready, G & 1, wc)) goto mma_done;
-          tc_fence_after();
-          fence_proxy_async_smem();
-          for (int v = 0; v < 2; ++v) {
-            if (!take(pv_unit(lo, j, r ^ 1, r, v))) goto mma_done;
-            issue_pv(v, false, true);
-            release();
-          }
-          mma_commit(&bars->pvp_done);
-          mma_commit_mc(&bars->pp_empty, peer_mask);  // the peer may write its next P here
         }
       }
     mma_done:
-      mma_commit(&bars->fin);
+      commit_local(&bars->fin);
       drain_wait(&bars->fin, 0, a.wait_limit_ns);
     }
     __syncwarp();
@@ -514,276 +544,356 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(prefix, a.B, k_begin, k_end);
       uint32_t st = 0, tofixph = 0;
       int sb, lo, hi;
+      const uint32_t fixed0 = cluster_addr(&bars->kv_fixed[0], 0);
       for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
         const int L = prefix[sb + 1] - prefix[sb];
         const int nr = (hi - lo + kRoundKeys - 1) / kRoundKeys;
-        const bool done = for_units(lo, nr, r, [&](const Unit& u, int) -> bool {
+        const bool done = for_units(lo, nr, r, [&](const Unit& u) -> bool {
+          if (u.rope_slot) return true;
           const uint32_t s = st;
           if (++st == kStages) st = 0;
           if (!needs_fix(u, L)) return true;
-          if (!warp_wait(&bars->kv_tofix[s], (tofixph >> s) & 1u, wc)) return false;
+          if (!warp_wait_cl(&bars->kv_tofix[s], (tofixph >> s) & 1u, wc)) return false;
           tofixph ^= 1u << s;
-          // rows [L - key0, 128) of both 64-dim blocks are past the sequence: zero them
-          const int r0 = max(L - u.key0, 0);
+          // rows [L - key0, 128) of both 64-dim boxes are past the sequence: zero them
+          const int r0 = min(max(L - u.key0, 0), RK);
           uint8_t* base = smem + kRingOff + s * kUnitBytes;
           for (int idx = lane; idx < (RK - r0) * 16; idx += 32) {
             const int row = r0 + (idx >> 4), b = (idx >> 3) & 1, c = idx & 7;
-            *reinterpret_cast<uint4*>(base + b * kBlockBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(base + b * kBoxBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->kv_fixed[s]);
+          if (lane == 0) arrive_cluster(fixed0 + s * 8);
           return true;
         });
         if (!done) break;
       }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int quad = warp & 3;
-    const int kh = (warp - 4) >> 2;  // which 64 of the CTA's 128 keys of a round
-    const int h = quad * 32 + lane;  // head = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const Msg* msg = reinterpret_cast<const Msg*>(smem + kMsgOff);
-    float* red_mx = reinterpret_cast<float*>(smem + kRedOff);            // [2 rounds][2 halves][NH]
-    float* red_l = reinterpret_cast<float*>(smem + kRedOff + 4 * NH * 4);  // [2 halves][NH]
-    const uint32_t peer = static_cast<uint32_t>(r ^ 1);
-    const uint32_t pp_peer = peer_addr(smem + kPPOff, peer) + kh * kBlockBytes + h * 128;
-    const uint32_t msg_peer = peer_addr(smem + kMsgOff, peer);
-    const uint32_t ppfull_peer = peer_addr(&bars->pp_full, peer);
-    uint8_t* pp_row = smem + kPPOff + kh * kBlockBytes + h * 128;
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ query RoPE, hand-offs to the even CTA
+    if (run) {
+      PieceIter it;
+      it.init(prefix, a.B, k_begin, k_end);
+      const uint32_t q_ready0 = cluster_addr(&bars->q_ready, 0);
+      const uint32_t pt_ready0 = cluster_addr(&bars->pt_ready, 0);
+      uint32_t gp = 0;
+      int sb, lo, hi;
+      for (uint32_t n = 0; it.next(&sb, &lo, &hi); ++n) {
+        const int L = prefix[sb + 1] - prefix[sb];
+        const int nr = (hi - lo + kRoundKeys - 1) / kRoundKeys;
+        if (!warp_wait_cl(&bars->q_full, n & 1, wc)) break;
+        if (f.n_pairs) {
+          // rotate dims [rope_offset, rope_offset + 2 n_pairs) of this CTA's 64 heads at the new token's position
+          const int c0 = a.rope_offset / 8;  // first 8-dim chunk of the span
+          for (int hl = lane; hl < HH; hl += 32) {
+            uint8_t* row = smem + kQOff + hl * 128;
+            auto chunk = [&](int c) {
+              return reinterpret_cast<uint4*>(row + (c >> 3) * kQBlockBytes + (((c & 7) ^ (hl & 7)) << 4));
+            };
+            if (f.half) {
+              for (int i = 0; i < f.n_pairs / 8; ++i) {
+                uint4* p0 = chunk(c0 + i);
+                uint4* p1 = chunk(c0 + i + f.n_pairs / 8);
+                float x0[8], x1[8];
+                bf16x8_to_f32(*p0, x0);
+                bf16x8_to_f32(*p1, x1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  float sn, cs;
+                  rope_sincos(L - 1, f.hi[i * 8 + e], f.lo[i * 8 + e], &sn, &cs);
+                  rotate_pair(x0[e], x1[e], sn, cs);
+                }
+                *p0 = f32_to_bf16x8(x0);
+                *p1 = f32_to_bf16x8(x1);
+              }
+            } else {
+              for (int i = 0; i < f.n_pairs / 4; ++i) {
+                uint4* ptr = chunk(c0 + i);
+                float x[8];
+                bf16x8_to_f32(*ptr, x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float sn, cs;
+                  rope_sincos(L - 1, f.hi[i * 4 + e], f.lo[i * 4 + e], &sn, &cs);
+                  rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
+                }
+                *ptr = f32_to_bf16x8(x);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) arrive_cluster(q_ready0);
+        if (r == 1) {
+          // this CTA's P^T of each round is complete (local rows + the even CTA's stores): make the stores
+          // visible to the tensor cores' reads and tell the issuer
+          bool ok = true;
+          for (int j = 0; j < nr; ++j, ++gp) {
+            if (!warp_wait_cl(&bars->pt_full, gp & 1, wc)) { ok = false; break; }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) arrive_cluster(pt_ready0);
+          }
+          if (!ok) break;
+        }
+      }
+    }
+  }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue (warps 4-11)
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int sw = warp - 4;            // softmax warp 0..7
+    const int qd = warp & 3;            // TMEM lane quarter: keys (S^T) / dims (O^T) 32 qd .. 32 qd + 31
+    const int hh = sw >> 2;             // heads [64 hh, 64 hh + 64)
+    const int key_l = 32 * qd + lane;   // this thread's key of the CTA's 128
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    float* red = reinterpret_cast<float*>(smem + kRedOff);        // [4][128]
+    float* mw = reinterpret_cast<float*>(smem + kMOff) + sw * HH;  // this warp's copy of the 64 offsets
+    float* facw = reinterpret_cast<float*>(smem + kFacOff) + sw * HH;  // this warp's rescale factors
+    float* l_cta = reinterpret_cast<float*>(smem + kLOff);
+    const float* l_peer = l_cta + NH;
+    int* flags = reinterpret_cast<int*>(smem + kFlagOff);          // [2][8]
+    const float* msg = reinterpret_cast<const float*>(smem + kMsgOff);
+    const uint32_t msg_peer = cluster_addr(smem + kMsgOff, peer);
+    const uint32_t msgbar_peer = cluster_addr(&bars->msg_full[0], peer);
+    const uint32_t lpeer_addr = cluster_addr(smem + kLOff + NH * 4, peer);
+    const uint32_t lbar_peer = cluster_addr(&bars->l_full, peer);
+    const uint32_t sfree0 = cluster_addr(&bars->s_free[0], 0);
+    const uint32_t oempty0 = cluster_addr(&bars->o_empty, 0);
+    // this thread's P^T row (key 128 r + key_l of the round) in the CTA that supplies heads [64 hh, +64)
+    const int prow = RK * r + key_l;
+    const bool pt_local = hh == r;
+    uint8_t* pt_row_local = smem + kPTOff + prow * 128;
+    const uint32_t pt_row_peer = cluster_addr(smem + kPTOff + prow * 128, peer);
+    const uint32_t ptbar_peer = cluster_addr(&bars->pt_full, peer);
     const float scl = a.scale_log2;
+    const bool owner = qd == 0;   // warps 4 and 8: lane owns heads 64 hh + lane and 64 hh + lane + 32
+    const bool armer = sw == 0 && lane == 0;
     PieceIter it;
     it.init(prefix, a.B, k_begin, k_end);
-    uint32_t G = 0, pvo_w = 0, pvp_w = 0, hs = 0;  // hs: uses of hsync[quad]
-    const bool armer = warp == 4 && lane == 0;  // arms pp_full for each later round's message
+    uint32_t g = 0, hs1 = 0, pvw = 0;
     int sb, lo, hi;
     for (uint32_t n = 0; run && it.next(&sb, &lo, &hi); ++n) {
-      const int L = prefix[sb + 1] - prefix[sb];
       const int nr = (hi - lo + kRoundKeys - 1) / kRoundKeys;
-      if (kh == 0) {
-        // query dims [0, 256) of head h -> TMEM columns [kQCol, kQCol + 128) as bf16 pairs (the
-        // A-operand layout: row = lane, two consecutive k per 32-bit column); the previous
-        // piece's score MMAs must have finished reading them
-        if (!warp_wait(&bars->q_empty, (n & 1) ^ 1, wc)) break;
-        tc_fence_after();
-        const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                           (static_cast<long long>(sb) * a.n_h + h) * DQK);
-#pragma unroll 1
-        for (int c = 0; c < kQTmemDims / 64; ++c) {  // 32 columns = 64 dims per store
-          uint32_t rq[32];
+      float lsum[HH];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 u = qrow[c * 8 + e];
-            rq[4 * e] = u.x;
-            rq[4 * e + 1] = u.y;
-            rq[4 * e + 2] = u.z;
-            rq[4 * e + 3] = u.w;
-          }
-          tmem_st32(tmem + lane_off + kQCol + c * 32, rq);
-        }
-        tmem_wait_st();
-        if (!warp_wait(&bars->q_full, n & 1, wc)) break;
-        if (f.n_pairs) {
-          // rotate this head's dims [rope_offset, rope_offset + rope_dims) (all in the shared-memory
-          // part) at the new token's position
-          uint8_t* row = smem + kQOff + h * 128;
-          auto chunk = [&](int c) {
-            return reinterpret_cast<uint4*>(row + (c >> 3) * kBlockBytes + (((c & 7) ^ (h & 7)) << 4));
-          };
-          const int c0 = (a.rope_offset - kQTmemDims) / 8;  // first chunk of the span
-          if (f.half) {
-            // pair j = span dims (j, j + n_pairs): chunk c0 + i holds first members, chunk c0 + i + n_pairs / 8
-            // the second ones (n_pairs % 8 == 0)
-            for (int i = 0; i < f.n_pairs / 8; ++i) {
-              uint4* p0 = chunk(c0 + i);
-              uint4* p1 = chunk(c0 + i + f.n_pairs / 8);
-              float x0[8], x1[8];
-              bf16x8_to_f32(*p0, x0);
-              bf16x8_to_f32(*p1, x1);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float sn, cs;
-                rope_sincos(L - 1, f.hi[i * 8 + e], f.lo[i * 8 + e], &sn, &cs);
-                rotate_pair(x0[e], x1[e], sn, cs);
-              }
-              *p0 = f32_to_bf16x8(x0);
-              *p1 = f32_to_bf16x8(x1);
-            }
-          } else {
-            for (int i = 0; i < f.n_pairs / 4; ++i) {
-              uint4* ptr = chunk(c0 + i);
-              float x[8];
-              bf16x8_to_f32(*ptr, x);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float sn, cs;
-                rope_sincos(L - 1, f.hi[i * 4 + e], f.lo[i * 4 + e], &sn, &cs);
-                rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
-              }
-              *ptr = f32_to_bf16x8(x);
-            }
-          }
-          fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->q_ready);
-      }
-
-      // m_sh: the pair's shared offset for the next round; m_O: the offset O and l are kept at
-      float m_sh = -INFINITY, m_O = -INFINITY, l_part = 0.f;
+      for (int c = 0; c < HH; ++c) lsum[c] = 0.f;
+      mw[lane] = kNoOffset;
+      mw[lane + 32] = kNoOffset;
+      __syncwarp();
       bool ok = true;
-      for (int j = 0; j < nr; ++j, ++G) {
-        const int own0 = lo + j * kRoundKeys + r * RK;
-        const int n_my = min(max(hi - own0 - 64 * kh, 0), 64);  // valid keys of this thread's 64
-        if (!warp_wait(&bars->s_full, G & 1, wc)) { ok = false; break; }
+      for (int j = 0; j < nr; ++j, ++g) {
+        const uint32_t buf = g & 1;
+        if (!warp_wait_cl(&bars->s_full[buf], (g >> 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[64];
-        tmem_ld32(tmem + lane_off + kSCol + 64 * kh, sr);
-        tmem_ld32(tmem + lane_off + kSCol + 64 * kh + 32, sr + 32);
+        uint32_t sr[HH];
+        tmem_ld32(tmem + lane_off + kSCol + 128 * buf + HH * hh, sr);
+        tmem_ld32(tmem + lane_off + kSCol + 128 * buf + HH * hh + 32, sr + 32);
         tmem_wait_ld();
-        float s[64];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_cluster(sfree0 + buf * 8);
+        const bool valid = lo + j * kRoundKeys + RK * r + key_l < hi;
+        float x[HH];
+        float dmax = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = (c < n_my) ? __uint_as_float(sr[c]) : -INFINITY;
-        // row maximum of this thread's keys: 8 chains of three-input max, then a tree
-        float m8[8];
+        for (int c = 0; c < HH; c += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mw + c);
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+          for (int e = 0; e < 4; ++e) {
+            x[c + e] = valid ? __uint_as_float(sr[c + e]) * scl : -INFINITY;
+            dmax = fmaxf(dmax, x[c + e] - mm[e]);
+          }
+        }
+        // does any score of this CTA pass its head's offset by 2^8?
+        const bool exceed = __any_sync(0xffffffffu, dmax > kRaise);
+        if (lane == 0) flags[buf * 8 + sw] = exceed ? 1 : 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->hsync[0]);  // one arrival per softmax warp
+        if (!warp_wait_cl(&bars->hsync[0], g & 1, wc)) { ok = false; break; }
+        int cta_exceed = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[24 + i], s[32 + i]);
+        for (int w = 0; w < 8; ++w) cta_exceed |= flags[buf * 8 + w];
+        float* mx_out = red;  // reused: per-quarter maxima, then read back
+        if (cta_exceed) {
+          // exact per-head maxima of this CTA's keys: over the warp's 32 keys, then the 4 quarters
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[40 + i], s[48 + i]);
+          for (int c = 0; c < HH; ++c) {
+            float v = x[c];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[56 + i]);
-        const float mx_my =
-            fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7])) * scl;
-        // the CTA's row maximum over its 128 keys (the two warps of these heads)
-        float* rm = red_mx + (G & 1) * 2 * NH;
-        rm[kh * NH + h] = mx_my;
-        mbar_arrive(&bars->hsync[quad]);
-        if (!warp_wait(&bars->hsync[quad], hs++ & 1, wc)) { ok = false; break; }
-        const float mx_cta = fmaxf(rm[h], rm[NH + h]);
-        const float m_own = mx_cta > m_sh + kEmergency ? mx_cta : m_sh;
-        uint32_t pr[32];
-        float rs = 0.f;
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if ((c & 31) == lane) red[qd * NH + HH * hh + c] = v;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->hsync[1]);
+          if (!warp_wait_cl(&bars->hsync[1], hs1++ & 1, wc)) { ok = false; break; }
+        }
+        // the message to the other CTA: the flag, and this CTA's maxima of the owner's two heads
+        if (owner) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = (2 * c < n_my) ? fast_exp2(fmaf(s[2 * c], scl, -m_own)) : 0.f;
-          const float p1 = (2 * c + 1 < n_my) ? fast_exp2(fmaf(s[2 * c + 1], scl, -m_own)) : 0.f;
-          rs += p0 + p1;
+          for (int e = 0; e < 2; ++e) {
+            const int h = HH * hh + lane + 32 * e;
+            float v = -INFINITY;
+            if (cta_exceed)
+              v = fmaxf(fmaxf(mx_out[h], mx_out[NH + h]), fmaxf(mx_out[2 * NH + h], mx_out[3 * NH + h]));
+            st_async_b32(msg_peer + (buf * kMsgWords + h) * 4, __float_as_uint(v), msgbar_peer + buf * 8);
+          }
+        }
+        if (sw == 0 && lane == 0)
+          st_async_b32(msg_peer + (buf * kMsgWords + NH) * 4, static_cast<uint32_t>(cta_exceed),
+                       msgbar_peer + buf * 8);
+        if (!warp_wait_cl(&bars->msg_full[buf], (g >> 1) & 1, wc)) { ok = false; break; }
+        const float* pm = msg + buf * kMsgWords;
+        const int peer_exceed = __float_as_int(pm[NH]);
+        // new offsets: where the pair's maximum passed a head's offset by 2^8, the offset moves to it; each
+        // lane decides its two columns, the warp reads them back after a __syncwarp
+        bool any_changed = false;
+        if (cta_exceed | peer_exceed) {
+          bool ch = false;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = lane + 32 * e, h = HH * hh + c;
+            float M = pm[h];
+            if (cta_exceed) M = fmaxf(M, fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h])));
+            const float mo = mw[c];
+            const float mn = M > mo + kRaise ? M : mo;
+            facw[c] = mn != mo ? fast_exp2(mo - mn) : 1.f;
+            ch |= mn != mo;
+            mw[c] = mn;
+          }
+          any_changed = __any_sync(0xffffffffu, ch);
+          __syncwarp();
+        }
+#pragma unroll
+        for (int c = 0; c < HH; c += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mw + c);
+          x[c] -= m4.x;
+          x[c + 1] -= m4.y;
+          x[c + 2] -= m4.z;
+          x[c + 3] -= m4.w;
+        }
+        if (any_changed) {
+#pragma unroll
+          for (int c = 0; c < HH; c += 4) {
+            const float4 f4 = *reinterpret_cast<const float4*>(facw + c);
+            lsum[c] *= f4.x;
+            lsum[c + 1] *= f4.y;
+            lsum[c + 2] *= f4.z;
+            lsum[c + 3] *= f4.w;
+          }
+        }
+        if (armer) mbar_arrive_expect_tx(&bars->msg_full[buf], kMsgBytes);  // round g + 2's message
+        // probabilities (bf16 pairs) and the running sums
+        uint32_t pr[HH / 2];
+#pragma unroll
+        for (int c = 0; c < HH / 2; ++c) {
+          const float p0 = fast_exp2(x[2 * c]);
+          const float p1 = fast_exp2(x[2 * c + 1]);
+          lsum[2 * c] += p0;
+          lsum[2 * c + 1] += p1;
           pr[c] = pack_bf16x2(p0, p1);
         }
-        // P (bf16 pairs) over the first 32 of this thread's 64 score columns
-        tmem_st32(tmem + lane_off + kSCol + 64 * kh, pr);
-        if (j == 0) {
-          m_O = m_own;  // P V(own) of the first round overwrites O
-          l_part = 0.f;
-        } else {
-          const bool resc = m_own > m_O;
-          if (__any_sync(0xffffffffu, resc)) {
-            // the previous P V(peer) is the last MMA that wrote O: let it finish, then move O to m_own
-            if (!warp_wait(&bars->pvp_done, pvp_w & 1, wc)) { ok = false; break; }
-            ++pvp_w;
-            tc_fence_after();
-            const float alpha = resc ? fast_exp2(m_O - m_own) : 1.f;
-            scale_o(tmem + lane_off + kOCol + 128 * kh, alpha);
-            l_part *= alpha;
-            if (resc) m_O = m_own;
+        // the previous round's P V has completed: P^T may be overwritten and O^T rescaled
+        if (j >= 1) {
+          if (!warp_wait_cl(&bars->pv_done, pvw & 1, wc)) { ok = false; break; }
+          ++pvw;
+          tc_fence_after();
+          if (any_changed) {
+            scale_cols64(tmem + lane_off + kOCol + HH * hh, facw);
+            scale_cols64(tmem + lane_off + kOCol + 128 + HH * hh, facw);
+            tmem_wait_st();
           }
         }
-        l_part += rs;
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_ready);
-
-        // this round's P, offset, maxima and sums -> the peer (its buffer is free once its
-        // previous P V(peer) has completed)
-        if (!warp_wait_cluster(&bars->pp_empty, (G & 1) ^ 1, wc)) { ok = false; break; }
+        // P^T row: heads [64 hh, +64) of this key, 128-byte swizzled, in the CTA that supplies those heads
+        if (pt_local) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_peer_v4(pp_peer + ((i ^ (h & 7)) << 4), pr[4 * i], pr[4 * i + 1], pr[4 * i + 2], pr[4 * i + 3],
-                     ppfull_peer);
-        if (kh == 0) {
-          st_peer_f32(msg_peer + h * 4, m_own, ppfull_peer);
-          st_peer_f32(msg_peer + (NH + h) * 4, mx_cta, ppfull_peer);
-        }
-        st_peer_f32(msg_peer + ((2 + kh) * NH + h) * 4, rs, ppfull_peer);
-
-        // the peer's round: bring O, l and the peer's P to one offset
-        if (!warp_wait_cluster(&bars->pp_full, G & 1, wc)) { ok = false; break; }
-        const float m_p = msg->m_own[h], mx_p = msg->mx[h], rs_p = msg->rs[kh][h];
-        // the next message may land only after this CTA's P V(peer) of this round has completed,
-        // which follows every thread's pp_ready below: arming the next phase here precedes it
-        if (armer) mbar_arrive_expect_tx(&bars->pp_full, kMsgBytes);
-        if (!warp_wait(&bars->pvo_done, pvo_w & 1, wc)) { ok = false; break; }
-        ++pvo_w;
-        if (pvp_w < G) {
-          if (!warp_wait(&bars->pvp_done, pvp_w & 1, wc)) { ok = false; break; }
-          ++pvp_w;
-        }
-        tc_fence_after();
-        const bool up = m_p > m_O;
-        if (__any_sync(0xffffffffu, up)) {
-          const float alpha = up ? fast_exp2(m_O - m_p) : 1.f;  // 0 when this CTA has no key yet (m_O = -inf)
-          scale_o(tmem + lane_off + kOCol + 128 * kh, alpha);
-          l_part *= alpha;
-          if (up) m_O = m_p;
-        }
-        float fp = 1.f;
-        if (m_p < m_O) {
-          fp = m_p == -INFINITY ? 0.f : fast_exp2(m_p - m_O);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint4* c = reinterpret_cast<uint4*>(pp_row + (i << 4));
-            float x[8];
-            bf16x8_to_f32(*c, x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] *= fp;
-            *c = f32_to_bf16x8(x);
-          }
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4*>(pt_row_local + ((i ^ (prow & 7)) << 4)) =
+                make_uint4(pr[4 * i], pr[4 * i + 1], pr[4 * i + 2], pr[4 * i + 3]);
           fence_proxy_async_smem();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_async_v4(pt_row_peer + ((i ^ (prow & 7)) << 4), pr[4 * i], pr[4 * i + 1], pr[4 * i + 2],
+                        pr[4 * i + 3], ptbar_peer);
         }
-        l_part += rs_p * fp;
-        const float mx_all = fmaxf(mx_cta, mx_p);
-        m_sh = mx_all > m_O + kRaise ? mx_all : m_O;
         tc_fence_before();
-        mbar_arrive(&bars->pp_ready);
+        __syncwarp();
+        if (lane == 0) {
+          if (sw == 0) mbar_arrive_expect_tx(&bars->pt_full, kPTPeerBytes);
+          else mbar_arrive(&bars->pt_full);
+        }
       }
       if (!__all_sync(0xffffffffu, ok)) break;
-      // epilogue: this piece's normalised partial for head h, value dims of this thread
-      if (!warp_wait(&bars->pvp_done, pvp_w & 1, wc)) break;
-      ++pvp_w;
+      // ---- epilogue: the piece's row sums over both CTAs, then O^T / l -> the partial of (pair, sequence)
+      if (!warp_wait_cl(&bars->pv_done, pvw & 1, wc)) break;
+      ++pvw;
       tc_fence_after();
-      red_l[kh * NH + h] = l_part;
-      mbar_arrive(&bars->hsync[quad]);
-      if (!warp_wait(&bars->hsync[quad], hs++ & 1, wc)) break;
-      const float l_tot = red_l[h] + red_l[NH + h];
-      const long long slot = static_cast<long long>(p) + sb;  // unique per (pair, sequence)
-      float* dst = a.ws_o + (slot * a.n_h + h) * DV + r * DVH + kh * 128;
-      const float inv_l = 1.f / l_tot;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t orow[32];
-        tmem_ld32(tmem + lane_off + kOCol + 128 * kh + c * 32, orow);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          reinterpret_cast<float4*>(dst + c * 32)[e] =
-              make_float4(__uint_as_float(orow[4 * e]) * inv_l, __uint_as_float(orow[4 * e + 1]) * inv_l,
-                          __uint_as_float(orow[4 * e + 2]) * inv_l, __uint_as_float(orow[4 * e + 3]) * inv_l);
+      for (int c = 0; c < HH; ++c) {
+        float v = lsum[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if ((c & 31) == lane) red[qd * NH + HH * hh + c] = v;
       }
-      if (r == 0 && kh == 0) a.ws_lse[slot * a.n_h + h] = m_O + log2f(l_tot);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->hsync[1]);
+      if (!warp_wait_cl(&bars->hsync[1], hs1++ & 1, wc)) break;
+      if (owner) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = HH * hh + lane + 32 * e;
+          const float v = (red[h] + red[NH + h]) + (red[2 * NH + h] + red[3 * NH + h]);
+          l_cta[h] = v;
+          st_async_b32(lpeer_addr + h * 4, __float_as_uint(v), lbar_peer);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->hsync[1]);
+      if (!warp_wait_cl(&bars->hsync[1], hs1++ & 1, wc)) break;
+      if (!warp_wait_cl(&bars->l_full, n & 1, wc)) break;
+      const long long slot = static_cast<long long>(p) + sb;  // unique per (pair, sequence)
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        const int dim = 256 * t + 128 * r + key_l;  // this thread's O^T row of tile t
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kOCol + 128 * t + HH * hh + 32 * cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int h = HH * hh + 32 * cc + e;
+            const float inv_l = 1.f / (l_cta[h] + l_peer[h]);
+            a.ws_o[(slot * a.n_h + h) * DV + dim] = __uint_as_float(o[e]) * inv_l;
+          }
+        }
+      }
+      if (r == 0 && owner) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = lane + 32 * e, h = HH * hh + c;
+          a.ws_lse[slot * a.n_h + h] = mw[c] + log2f(l_cta[h] + l_peer[h]);
+        }
+      }
       tc_fence_before();
-      mbar_arrive(&bars->o_empty);
+      __syncwarp();
+      // the next piece's sums may land once its phase is armed (not before every thread of this CTA has
+      // finished this piece's rounds, which the other CTA's next epilogue waits for)
+      if (armer) mbar_arrive_expect_tx(&bars->l_full, NH * 4);
+      if (lane == 0) arrive_cluster(oempty0);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while the other may still write its shared memory
+  cluster_sync();  // no CTA leaves while the other may still use its shared memory or TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
 }
 
@@ -873,8 +983,8 @@ bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long
 }
 
 bool decode_mla_rope_ok(int rope_offset, int rope_dims, bool half) {
-  // the rotated span lies in the shared-memory part of the query, in whole 8-dim chunks
-  return rope_offset >= kQTmemDims && rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0;
+  // the query lives in shared memory: the rotated span must be whole 8-dim chunks
+  return rope_offset % 8 == 0 && rope_dims % (half ? 16 : 8) == 0 && rope_offset + rope_dims <= DQK;
 }
 
 namespace {
@@ -884,8 +994,12 @@ std::atomic<int> g_mla_pairs[32];      // per device: clusters of two CTAs that 
 cudaError_t mla_prepare(int dev) {
   const unsigned bit = 1u << (dev & 31);
   if (g_mla_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the register split must fit the registers the compiled kernel launches with
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, mla_decode_kernel);
+  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(fa.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   g_mla_ready.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;

@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_stream_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ RopeFreq f,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the shared array, so that the compiler keeps shared-memory addressing
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   float* red_o = reinterpret_cast<float*>(smem + kRedOff);  // [16][HG][D]
   float* red_m = red_o + 16 * HG * D;                        // [16][HG]

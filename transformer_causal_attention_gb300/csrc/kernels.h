@@ -106,7 +106,6 @@ cudaError_t launch_decode(const DecodeArgs& a, const RopeFreq& rope, bool bf16, 
 cudaError_t launch_decode_combine(const DecodeArgs& a, bool bf16, cudaStream_t st, int* launches);
 constexpr int kMlaMaxPairs = 128;  // CTA pairs of the MLA decode kernel (workspace is sized for this)
 constexpr int kMlaTileKeys = 128;  // keys per CTA per round (TMA box rows) of the MLA decode kernel
-constexpr int kMlaQTmemDims = 256; // query dims [0, kMlaQTmemDims) held in TMEM
 bool decode_mla_supported(int B, int n_h, int n_kv, int D_qk, int D_v, long long v_token_stride, bool v_is_k,
                           bool bf16);
 int decode_mla_pairs(int num_sms);
