@@ -490,15 +490,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < kQkUnits; ++u) {
               const Unit un = qk_unit(lo, j, 0, u);
               if (!take(un)) goto mma_done;
-              const uint32_t base = un.rope_slot ? smem_u32(smem + kRopeOff) : smem_u32(smem + kRingOff + st * kUnitBytes);
-              for (int b = 0; b < un.nbox; ++b) {
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                  const int qb = 2 * u + b;  // 64-dim block of the query
-                  mma_pair(tmem + kSCol + 128 * buf, sdesc_sw128(base + b * kBoxBytes + k4 * 32, 16, 1024),
-                           sdesc_sw128(q_addr + qb * kQBlockBytes + k4 * 32, 16, 1024), kIdescQK,
-                           (u | b | k4) ? 1u : 0u);
-                }
+              // descriptors of the unit's first 16 dims; the rest differ only in the start address (+32 bytes
+              // per 16 dims = +2 in the descriptor, + one box per 64 dims).  The pair MMA holds the issuing
+              // thread until it is handed on, so nothing but the MMAs sits between them.
+              const uint64_t a0 = sdesc_sw128(un.rope_slot ? smem_u32(smem + kRopeOff)
+                                                           : smem_u32(smem + kRingOff + st * kUnitBytes), 16, 1024);
+              const uint64_t b0 = sdesc_sw128(q_addr + 2 * u * kQBlockBytes, 16, 1024);
+              const uint32_t dS = tmem + kSCol + 128 * buf;
+              mma_pair(dS, a0, b0, kIdescQK, u ? 1u : 0u);
+              mma_pair(dS, a0 + 2, b0 + 2, kIdescQK, 1u);
+              mma_pair(dS, a0 + 4, b0 + 4, kIdescQK, 1u);
+              mma_pair(dS, a0 + 6, b0 + 6, kIdescQK, 1u);
+              if (un.nbox == 2) {
+                constexpr uint64_t kA = kBoxBytes >> 4, kB = kQBlockBytes >> 4;
+                mma_pair(dS, a0 + kA, b0 + kB, kIdescQK, 1u);
+                mma_pair(dS, a0 + kA + 2, b0 + kB + 2, kIdescQK, 1u);
+                mma_pair(dS, a0 + kA + 4, b0 + kB + 4, kIdescQK, 1u);
+                mma_pair(dS, a0 + kA + 6, b0 + kB + 6, kIdescQK, 1u);
               }
               release(un);
             }
@@ -517,13 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int t = 0; t < 2; ++t) {
                 const Unit un = pv_unit(lo, j - 1, 0, kh, t);
                 if (!take(un)) goto mma_done;
-                const uint32_t vaddr = smem_u32(smem + kRingOff + st * kUnitBytes);
+                // 16 keys per MMA: +16 rows of 128 bytes = +128 in both descriptors
+                const uint64_t a0 = sdesc_sw128(smem_u32(smem + kRingOff + st * kUnitBytes), kBoxBytes, 1024);
+                const uint64_t b0 = sdesc_sw128(pt_addr + kh * RK * 128, kBoxBytes, 1024);
+                const uint32_t dO = tmem + kOCol + 128 * t;
+                mma_pair(dO, a0, b0, kIdescPV, (j > 1 || kh > 0) ? 1u : 0u);
 #pragma unroll
-                for (int i = 0; i < RK / 16; ++i) {
-                  mma_pair(tmem + kOCol + 128 * t, sdesc_sw128(vaddr + i * 16 * 128, kBoxBytes, 1024),
-                           sdesc_sw128(pt_addr + (kh * RK + i * 16) * 128, kBoxBytes, 1024), kIdescPV,
-                           (j > 1 || kh > 0 || i > 0) ? 1u : 0u);
-                }
+                for (int i = 1; i < RK / 16; ++i) mma_pair(dO, a0 + 128 * i, b0 + 128 * i, kIdescPV, 1u);
                 release(un);
               }
             }
