@@ -57,7 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # DRAM bytes (read + write) per launch of the prefill kernel on the benchmark
 # workload, from an ncu capture of one launch; valid only for the kernel source
 # it was taken on (sha256 of prefill_tc.cu, first 16 hex digits), else null.
-PREFILL_TRAFFIC = {"kernel_sha": "b2e7ceb98e6dc36d", "bytes": 4 * 127.557e6, "scaled_from_b1": True}
+PREFILL_TRAFFIC = {"kernel_sha": "a17b15cebd638ade", "bytes": 1.65e9 + 226.88e6}
 
 
 def kernel_sha(name: str) -> str:
@@ -377,8 +377,6 @@ def run_ours(args):
                 "frac": per_gpu_prefill / bf16_peak, "traffic": traffic,
                 "kernel": "attn_prefill (RoPE-K pass + prefill_tc_kernel<128>)",
                 "peak_source": f"{peak_kind} bf16 burst"}
-    if traffic is not None and PREFILL_TRAFFIC.get("scaled_from_b1"):
-        roofline["traffic_note"] = "B=1 capture scaled by 4 (L2 held part of a B=1 launch's bytes)"
 
     # ---- end to end through the public API: pinned host inputs in, result out, every step.
     # The batch is pipelined per sequence over three streams: the copy-in of
