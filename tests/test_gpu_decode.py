@@ -139,6 +139,48 @@ def test_mla_decode_batch_limit(lib, B):
     assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
 
 
+@pytest.mark.parametrize("lens,rope", [
+    ([1], 0.0),              # one key in all: every CTA pair but one has nothing to do
+    ([1, 2], 1e4),
+    ([3, 1, 1], 0.0),
+    ([257], 1e4),            # a second round holding a single valid key
+    ([255, 1, 256], 0.0),
+])
+def test_mla_decode_few_keys(lib, lens, rope):
+    # far fewer keys than CTA pairs x 256: most pairs get an empty key range, and the partials
+    # of the pairs that do get keys must still combine to each sequence's result
+    L = max(lens)
+    cfg = workloads.config("mla_decode", B=len(lens), max_len=L, len_lo=1, len_hi=L, rope_base=rope)
+    q, kc, vc, _ = workloads.decode_inputs(cfg, seed=L + len(lens))
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out, lse = run_decode(lib, cfg, q, kc, vc, sl)
+    ref, ref_lse = oracle_decode(cfg, q, kc, vc, sl)
+    assert_parity(out, ref, "bf16", f"mla decode lens={lens}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
+@pytest.mark.parametrize("roff,rdims,pairing", [
+    (0, 64, "adjacent"),     # span at the start of the latent (inside the value dims)
+    (256, 128, "half"),
+    (504, 72, "adjacent"),   # span across the end of the value dims
+    (64, 256, "half"),       # the widest span
+])
+def test_mla_decode_rope_spans(lib, roff, rdims, pairing):
+    # the tensor-core MLA kernel rotates the query in shared memory, any span of whole 8-dim chunks
+    cfg = workloads.config("mla_decode", B=3, max_len=600, len_lo=1, len_hi=600, rope_base=1e4)
+    q, kc, vc, sl = workloads.decode_inputs(cfg, seed=roff + rdims)
+    sl[0] = 1
+    sl[-1] = 600
+    kd = kc.to(DEV)
+    out, lse = lib.decode(q.to(DEV), kd, kd[..., :512], sl.to(DEV), rope_base=1e4, rope_offset=roff,
+                          rope_dims=rdims, scale=cfg["scale"], lse=True, pairing=pairing)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.attention_decode(q, kc, vc, sl.numpy(), rope_base=1e4, rope_offset=roff,
+                                           rope_dims=rdims, scale=cfg["scale"], pairing=pairing)
+    assert_parity(out, ref, "bf16", f"mla decode rope [{roff}, {roff + rdims}) {pairing}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) <= BF16_MAX_ABS
+
+
 def test_mla_shaped_decode_fp32(lib):
     # the tensor-core MLA kernel is bf16; fp32 inputs of the same shape run on the generic kernel
     cfg = workloads.config("mla_decode", B=2, max_len=200, len_lo=1, len_hi=200, rope_base=1e4, dtype="f32")
