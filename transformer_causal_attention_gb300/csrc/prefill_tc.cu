@@ -425,7 +425,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars->k_empty[kst]);
           if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+          // Loaded tiles [vs, ve): both Q tiles take P V(j) and Q K(j + 1), neither at its first
+          // P V or Q K.  They run through a loop without per-tile decisions: every instruction of
+          // the issuing lane between two bursts is time the tensor pipe waits (a clock trace of
+          // the general loop showed ~1600 of its ~4200 cycles per key tile spent there).
+          int vs = itm.n_load, ve = itm.n_load;
+          if (itm.ns_u == 0) {  // loaded tiles are r0.jl + v
+            vs = itm.r1.jl - itm.r0.jl + 1;
+            ve = itm.r0.jh - itm.r0.jl;
+          }
           for (int v = 0; v < itm.n_load; ++v) {
+            if (v == vs && vs < ve) {
+              for (; v < ve; ++v) {
+                if (!mbar_wait(&bars->p_full[0], pph0, wc)) goto mma_done;
+                if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+                if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
+                pph0 ^= 1;
+                tc_fence_after();
+                issue_pv(0, vst, true);
+                issue_qk(0, qs0, kst);
+                mma_commit(&bars->s_full[0]);
+                if (!mbar_wait(&bars->p_full[1], pph1, wc)) goto mma_done;
+                pph1 ^= 1;
+                tc_fence_after();
+                issue_pv(1, vst, true);
+                mma_commit(&bars->v_empty[vst]);
+                if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
+                issue_qk(1, qs1, kst);
+                mma_commit(&bars->s_full[1]);
+                mma_commit(&bars->k_empty[kst]);
+                if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+              }
+            }
             const int j = itm.load_at(v);
             const bool next = v + 1 < itm.n_load;
             const int jn = next ? itm.load_at(v + 1) : -1;
