@@ -14,12 +14,8 @@
 //               shared-memory stages (128-byte swizzle).
 //   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
 //               S_t = Q_t K_j^T (A, B from shared memory) and O_t += P_t V_j
-//               (P read from TMEM, V from shared memory as an MN-major operand).
-//               A tcgen05.mma is accepted only as the tensor pipe frees a slot,
-//               so the lane does every wait of a tile first and then issues its
-//               P V and Q K as one burst.  (One issuing lane per Q tile was
-//               measured 15% slower: the two tiles' MMAs then interleave and
-//               each tile's chain through its softmax gets longer.)
+//               (P read from TMEM, V from shared memory as an MN-major operand),
+//               each tile's P V and next Q K as one burst.
 //   warp 3      idle (gives its registers to the softmax warpgroups)
 //   warps 4-7   softmax warpgroup of Q tile 0, warps 8-11 of Q tile 1: each thread
 //               owns one query row (TMEM lane), so row max / row sum need no
@@ -60,7 +56,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // waits until the pool has the registers, so the split must fit the pool; the
 // launcher checks the compiled register count against it before launching.
 constexpr int kLaunchRegs = 168;
-constexpr int kRegsCtl = 136, kRegsSoftmax = 184;
+constexpr int kRegsCtl = 152, kRegsSoftmax = 176;  // 136 / 184 left the issuer of D_qk = 192 spilling
 constexpr int kRegsNeeded = 4 * 32 * kRegsCtl + 8 * 32 * kRegsSoftmax;
 static_assert(kRegsNeeded <= kThreads * kLaunchRegs, "register split exceeds the launch's pool");
 
@@ -95,12 +91,13 @@ struct Cfg {
 
 struct Bars {
   uint64_t q_full[3], q_ready[3], q_empty[3];  // per Q slot
-  uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
+  uint64_t s_full[2], p_half[2], p_full[2], o_done[2], o_empty[2];
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];  // up to 3 stages
   uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Key tiles of one Q tile: [0, ns) (attention-sink tiles kept outside the
 // window) followed by [jl, jh] (the window up to the diagonal).  Without a
@@ -276,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_half[t], 128);
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_empty[t], 128);
@@ -383,6 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // One lane issues both tiles' MMAs.  Per loaded key tile j: for each Q tile
       // t that needs it, every wait first (P_t(j) ready, K(j+1) landed), then
       // P_t V(j) and Q_t K(j+1) back to back, so the tensor pipe sees one burst.
+      // An MMA instruction holds the lane ~53 cycles (measured), nearly the 64 cycles
+      // it occupies the pipe, so every other instruction of the lane between bursts is
+      // time the pipe may wait.  (One lane per Q tile measured 17% slower: the two tiles'
+      // MMAs then interleave in the pipe and each tile's chain through its softmax grows.)
       if (lane == 0) {
         const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem(0)), 16, 1024);
         const uint64_t k_desc0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
@@ -390,22 +392,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph0 = 0, pph1 = 0;
         uint32_t it = 0;
         uint32_t qs0 = 0, qp0 = 0;  // slot and parity of Q tile 0 of the current item
-        auto issue_qk = [&](int t, uint32_t qslot, uint32_t stage) {
+        // Q_t K over the dims [DQK/2 * half, DQK/2 * (half + 1)), or all dims (half < 0)
+        auto issue_qk_part = [&](int t, uint32_t qslot, uint32_t stage, int half) {
           const uint64_t a0 = q_desc0 + ((qslot * C::kQKTileBytes) >> 4);
           const uint64_t b0 = k_desc0 + ((stage * C::kQKTileBytes) >> 4);
+          const int k_lo = half > 0 ? DQK / 32 : 0, k_hi = half == 0 ? DQK / 32 : DQK / 16;
 #pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk) {
+          for (int kk = k_lo; kk < k_hi; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBlockBytes + (kk & 3) * 32) >> 4;
             mma_ss(tmem + t * 128u, a0 + off, b0 + off, C::kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+        auto issue_qk = [&](int t, uint32_t qslot, uint32_t stage) { issue_qk_part(t, qslot, stage, -1); };
+        // P_t V over the keys [64 half, 64 half + 64) of the tile (P of those keys sits in TMEM
+        // columns [32 half, 32 half + 32) of the tile's S columns, two bf16 per column)
+        auto issue_pv_half = [&](int t, uint32_t stage, bool accumulate, int half) {
           const uint64_t b0 = v_desc0 + ((stage * C::kVTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
+          for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
+        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+          issue_pv_half(t, stage, accumulate, 0);
+          issue_pv_half(t, stage, accumulate, 1);
+        };
+        static_assert(BN == 128, "P V is issued in two halves of 64 keys");
         for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
           const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
@@ -436,25 +448,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int v = 0; v < itm.n_load; ++v) {
             if (v == vs && vs < ve) {
+              // V(j) and K(j + 1) of the first iteration; each iteration then waits for the next
+              // one's while the tensor pipe still holds its own last MMAs
+              if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+              if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
               for (; v < ve; ++v) {
+                // the softmax hands over P in two halves of 64 keys: the first half's P V runs
+                // while it computes the second half
+                if (!mbar_wait(&bars->p_half[0], pph0, wc)) goto mma_done;
+                if (C::kVStages == 1 && !mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+                tc_fence_after();
+                issue_pv_half(0, vst, true, 0);
                 if (!mbar_wait(&bars->p_full[0], pph0, wc)) goto mma_done;
-                if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
-                if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
                 pph0 ^= 1;
                 tc_fence_after();
-                issue_pv(0, vst, true);
+                issue_pv_half(0, vst, true, 1);
                 issue_qk(0, qs0, kst);
                 mma_commit(&bars->s_full[0]);
+                if (!mbar_wait(&bars->p_half[1], pph1, wc)) goto mma_done;
+                tc_fence_after();
+                issue_pv_half(1, vst, true, 0);
                 if (!mbar_wait(&bars->p_full[1], pph1, wc)) goto mma_done;
                 pph1 ^= 1;
                 tc_fence_after();
-                issue_pv(1, vst, true);
+                issue_pv_half(1, vst, true, 1);
                 mma_commit(&bars->v_empty[vst]);
                 if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
-                issue_qk(1, qs1, kst);
+                issue_qk_part(1, qs1, kst, 0);
+                uint32_t kst_n = kst + 1, kph_n = kph;
+                if (kst_n == static_cast<uint32_t>(C::kKStages)) { kst_n = 0; kph_n ^= 1; }
+                if (v + 1 < ve) {
+                  // (with one V stage the next V tile only starts loading now: it is waited for at
+                  // the top of the next iteration instead)
+                  if (C::kVStages > 1 && !mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+                  if (!mbar_wait(&bars->k_full[kst_n], kph_n, wc)) goto mma_done;
+                }
+                issue_qk_part(1, qs1, kst, 1);
                 mma_commit(&bars->s_full[1]);
                 mma_commit(&bars->k_empty[kst]);
-                if (++kst == C::kKStages) { kst = 0; kph ^= 1; }
+                kst = kst_n;
+                kph = kph_n;
               }
             }
             const int j = itm.load_at(v);
@@ -466,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const TileRange& r = t ? itm.r1 : itm.r0;
               const bool pv = r.has(j), qk = next && r.has(jn);
               if (pv) {
+                if (!mbar_wait(&bars->p_half[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (!mbar_wait(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (t) pph1 ^= 1; else pph0 ^= 1;
                 if (!(t ? pv_seen1 : pv_seen0) && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
@@ -588,14 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // operations would dominate the warp's latency
         float m8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+        for (int e = 0; e < 8; ++e) m8[e] = s[e];
         static_assert((BN - 8) % 16 == 8, "chains take 16 columns per round plus one round of 8");
 #pragma unroll
         for (int c = 8; c + 16 <= BN; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+          for (int e = 0; e < 8; ++e) m8[e] = fmax3(m8[e], s[c + e], s[c + 8 + e]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BN - 8 + i]);
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[BN - 8 + e]);
         const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7])) *
                          a.scale_log2;
         // Move to a new reference maximum only when the row maximum grew by more
@@ -608,7 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
         // p = 2^(s * scale*log2e - m), two columns per packed fp32x2 FMA; the row
-        // sum runs in 4 independent packed accumulators
+        // sum runs in 4 independent packed accumulators.  P goes back to TMEM in two
+        // halves of 64 keys, each announced on its own barrier, so that the MMA issuer
+        // runs the first half's P V while the second half is computed.
         uint32_t pr[BN / 2];
         const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
         // a row whose tiles so far held no visible key keeps m = -inf: its
@@ -617,20 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 nm2 = make_float2(-m_ref, -m_ref);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
+        for (int c = 0; c < BN / 4; ++c) {
           const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           acc[c & 3] = __fadd2_rn(acc[c & 3], pp);
           pr[c] = pack_bf16x2(pp.x, pp.y);
         }
-        acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        l_run += acc[0].x + acc[0].y;
         tmem_st32(s_addr, pr);
-        tmem_st32(s_addr + 32, pr + 32);
-        // O rescale, once the scores are dead (fewer live registers).  P V(j-1)
-        // has completed (s_full of tile j was committed after it), P V(j) waits
-        // for p_full below.  TMEM loads/stores are warp-collective: the whole
-        // warp rescales when any of its rows needs it (alpha is 1 for the others).
+        // O rescale before the first P V of this tile accumulates into O.  P V(j-1) has
+        // completed (s_full of tile j was committed after it).  TMEM loads/stores are
+        // warp-collective: the whole warp rescales when any of its rows needs it (alpha
+        // is 1 for the others).
         if (__any_sync(0xffffffffu, need && i > 0)) {
 #pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
@@ -642,6 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_addr + c * 32, orow);
           }
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_half[t]);
+#pragma unroll
+        for (int c = BN / 4; c < BN / 2; ++c) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[c & 3] = __fadd2_rn(acc[c & 3], pp);
+          pr[c] = pack_bf16x2(pp.x, pp.y);
+        }
+        acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l_run += acc[0].x + acc[0].y;
+        tmem_st32(s_addr + 32, pr + 32);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
