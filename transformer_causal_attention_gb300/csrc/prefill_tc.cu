@@ -81,7 +81,8 @@ struct Cfg {
   static constexpr int kKOff = kQOff + kQSlots * kQKTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kQKTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kVTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
+  static constexpr int kFreqOff = kBarOff + 512;  // the RoPE frequencies, hi then lo words
+  static constexpr int kSmemBytes = kFreqOff + 2 * kMaxRopePairs * 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kOCol0 = 256;         // S of the two tiles in columns [0, 256)
   static_assert(kOCol0 + 2 * DV <= 512, "TMEM columns");
@@ -203,18 +204,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // 128 rows x 128 bytes with the 128-byte swizzle: the 16-byte chunk c of row r
 // sits at chunk (c & 7) ^ (r & 7) of block c >> 3.  rope_offset is a multiple
 // of 8 (whole chunks).  Kept out of line: it runs once per tile row, and inlined
-// it costs the softmax loop registers.  Its sin/cos come from rope_sincos_fast:
+// it costs the softmax loop registers.  The frequencies come from shared memory:
+// read through a reference to the kernel parameter, out of line, the rotation of
+// one tile took ~8000 cycles (a clock trace), about four times its arithmetic.
+// Its sin/cos come from rope_sincos_fast:
 // with the accurate pair the rotation of each new item's Q tile measured 7% of
 // the Llama-3-8B prefill (it runs between two items, while the tensor pipe waits).
 template <int DQK>
-__device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope_offset, const RopeFreq& f) {
+__device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope_offset, int n_pairs, bool half,
+                                        const float* f_hi, const float* f_lo) {
   constexpr int kBlockBytes = BM * 128;
   auto chunk = [&](int c) -> uint8_t* { return row + (c >> 3) * kBlockBytes + (((c & 7) ^ (r & 7)) << 4); };
   const int c0 = rope_offset / 8;
-  if (f.half) {
+  if (half) {
     // pair j = span dims (j, j + n_pairs): chunk c0 + i holds the first members of
     // pairs 8i..8i+7, chunk c0 + i + n_pairs / 8 their second members
-    const int hc = f.n_pairs / 8;
+    const int hc = n_pairs / 8;
 #pragma unroll 1
     for (int i = 0; i < hc; ++i) {
       uint4* p0 = reinterpret_cast<uint4*>(chunk(c0 + i));
@@ -225,7 +230,7 @@ __device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float sn, cs;
-        rope_sincos_fast(pos, f.hi[i * 8 + e], f.lo[i * 8 + e], &sn, &cs);
+        rope_sincos_fast(pos, f_hi[i * 8 + e], f_lo[i * 8 + e], &sn, &cs);
         rotate_pair(x0[e], x1[e], sn, cs);
       }
       *p0 = f32_to_bf16x8(x0);
@@ -233,14 +238,14 @@ __device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope
     }
   } else {
 #pragma unroll 1
-    for (int i = 0; i < f.n_pairs / 4; ++i) {
+    for (int i = 0; i < n_pairs / 4; ++i) {
       uint4* p = reinterpret_cast<uint4*>(chunk(c0 + i));
       float x[8];
       bf16x8_to_f32(*p, x);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float sn, cs;
-        rope_sincos_fast(pos, f.hi[i * 4 + e], f.lo[i * 4 + e], &sn, &cs);
+        rope_sincos_fast(pos, f_hi[i * 4 + e], f_lo[i * 4 + e], &sn, &cs);
         rotate_pair(x[2 * e], x[2 * e + 1], sn, cs);
       }
       *p = f32_to_bf16x8(x);
@@ -258,6 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // aligned by pointer arithmetic on the shared array, so that the compiler keeps shared-memory addressing
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+  float* const f_hi = reinterpret_cast<float*>(smem + C::kFreqOff);
+  float* const f_lo = f_hi + kMaxRopePairs;
+  for (int i = threadIdx.x; i < f.n_pairs; i += kThreads) {  // made visible by the __syncthreads below
+    f_hi[i] = f.hi[i];
+    f_lo[i] = f.lo[i];
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_qt = (a.S + BM - 1) / BM;
@@ -565,7 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
       if (f.n_pairs) {
         const Item nx = decode_item<FOLD>(item_idx, a, n_pairs_q, n_kt);
-        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t) * BM + r, a.rope_offset, f);
+        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t) * BM + r, a.rope_offset, f.n_pairs,
+                          f.half != 0, f_hi, f_lo);
         fence_proxy_async_smem();
       }
       mbar_arrive(&bars->q_ready[qs]);
