@@ -45,9 +45,27 @@ __device__ __forceinline__ void store_chunk(T* p, const float* x) {
 // Rotate n_rows rows (stride `stride` elements) of the chunk at span-relative
 // dim `rel` from src to dst at position pos.  The caller skips chunks of the
 // second half in the split-halves layout (their owner is rel - n_pairs).
+// The frequencies of the rotation (hi and lo words, n_pairs each) sit in shared memory: every
+// thread reads those of its own chunk, and lanes with different chunks read different words,
+// which a kernel-parameter array would serve one address at a time.
+struct SmemFreq {
+  const float* hi;
+  const float* lo;
+  int n_pairs;
+  bool half;
+};
+__device__ __forceinline__ SmemFreq stage_freq(const RopeFreq& f, float* buf) {
+  for (int i = threadIdx.x; i < f.n_pairs; i += blockDim.x) {
+    buf[i] = f.hi[i];
+    buf[kMaxRopePairs + i] = f.lo[i];
+  }
+  __syncthreads();
+  return SmemFreq{buf, buf + kMaxRopePairs, f.n_pairs, f.half != 0};
+}
+
 template <typename T, int CH>
 __device__ __forceinline__ void rotate_chunk_rows(const T* src, T* dst, long long stride, int n_rows, int rel, int pos,
-                                                  const RopeFreq& f) {
+                                                  const SmemFreq& f) {
   if (f.half) {
     float sn[CH], cs[CH];
 #pragma unroll
@@ -76,7 +94,9 @@ __device__ __forceinline__ void rotate_chunk_rows(const T* src, T* dst, long lon
 }
 
 template <typename T, int CH>
-__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq f) {
+__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq rf) {
+  __shared__ float freq[2 * kMaxRopePairs];
+  const SmemFreq f = stage_freq(rf, freq);
   const int chunks = a.D / CH;
   const long long total = static_cast<long long>(a.B) * a.S * chunks;
   const T* in = static_cast<const T*>(a.in);
@@ -112,7 +132,9 @@ template <typename T>
 // the GPU's loads in flight when each thread walks all heads one after another, so the
 // launcher then gives every head its own thread (head_groups = n_kv; each thread computes
 // its own sin/cos), and otherwise one thread per (token, chunk) for all heads.
-__global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq f) {
+__global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq rf) {
+  __shared__ float freq[2 * kMaxRopePairs];
+  const SmemFreq f = stage_freq(rf, freq);
   const int kch = a.D_qk / 8, vch = a.v_new ? a.D_v / 8 : 0;
   const int per_tok = kch + vch;
   const int hg = a.head_groups, hpt = a.n_kv / hg;  // heads per thread
