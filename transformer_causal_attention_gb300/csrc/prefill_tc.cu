@@ -452,11 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P V or Q K.  They run through a loop without per-tile decisions: every instruction of
           // the issuing lane between two bursts is time the tensor pipe waits (a clock trace of
           // the general loop showed ~1600 of its ~4200 cycles per key tile spent there).
-          int vs = itm.n_load, ve = itm.n_load;
-          if (itm.ns_u == 0) {  // loaded tiles are r0.jl + v
-            vs = itm.r1.jl - itm.r0.jl + 1;
-            ve = itm.r0.jh - itm.r0.jl;
-          }
+          // (the window part of the loaded tiles: tile r0.jl + v - ns_u at v >= ns_u; sink tiles, when
+          // there are any, are in both Q tiles' ranges and come first)
+          const int vs = itm.ns_u + itm.r1.jl - itm.r0.jl + 1;
+          const int ve = itm.ns_u + itm.r0.jh - itm.r0.jl;
           for (int v = 0; v < itm.n_load; ++v) {
             if (v == vs && vs < ve) {
               // V(j) and K(j + 1) of the first iteration; each iteration then waits for the next
