@@ -118,6 +118,8 @@ def test_append_then_decode_matches_prefill_last_row(lib):
     (1, 700, 4, 2, 128, 256, 4, "bf16"),    # window of 2 key tiles, 4 sinks (tensor cores)
     (2, 520, 2, 1, 64, 300, 0, "bf16"),     # unaligned window, no sinks: rows whose first tile is all masked
     (1, 400, 2, 2, 128, 1000, 4, "bf16"),   # window longer than the prompt: plain causal
+    (1, 2048, 4, 2, 128, 1024, 4, "bf16"),  # long enough for the issuer's steady loop after a sink tile
+    (1, 1536, 2, 1, 64, 512, 130, "bf16"),  # two sink tiles, then the steady loop
     (1, 333, 2, 2, 96, 100, 7, "bf16"),     # CUDA-core path
     (1, 90, 2, 2, 16, 20, 3, "f32"),
 ])
