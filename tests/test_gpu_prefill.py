@@ -114,6 +114,28 @@ def test_llama_config_every_slice(lib):
         assert_parity(krot_c[b], oracle.rope_cache(k[b:b + 1], cfg["rope_base"])[0], "bf16", f"llama k_rot b={b}")
 
 
+def test_folded_dealing_d128_every_slice(lib):
+    # K/V of 3 x 24 heads x 8192 keys (302 MB) is over twice the L2 and there are more than four
+    # waves of double items, so the D = 128 kernel deals (heavy, light) tile pairs of one head
+    # together; every slice at every Q tile's first and last row must match the oracle
+    cfg = dict(B=3, S=8192, n_h=24, n_kv=24, D_h=128, dtype="bf16", rope_base=5e5, scale=0.0)
+    q, k, v = workloads.prefill_inputs(cfg, seed=21)
+    out, _, lse = gpu_prefill(lib, cfg, q, k, v)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    del out, lse
+    rows = tile_edge_rows(cfg["S"])
+    got, want, worst_lse = [], [], 0.0
+    for b in range(cfg["B"]):
+        for h in range(cfg["n_h"]):
+            ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, rows, rope_base=cfg["rope_base"],
+                                                         scale=None)
+            got.append(to_np(out_c[b, rows, h]))
+            want.append(ref)
+            worst_lse = max(worst_lse, float(np.max(np.abs(to_np(lse_c[b, h, rows]) - ref_lse))))
+    assert worst_lse <= BF16_MAX_ABS, f"lse max-abs {worst_lse}"
+    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", "folded D=128 prefill, every slice")
+
+
 def test_online_softmax_rescale_branch(lib):
     # scores grow by ~17 (log2 units) from one key tile to the next, so the
     # running maximum moves past the lazy-rescale threshold on every tile
