@@ -2,10 +2,12 @@
 
 "Transformer 与 LLM" slide 06: prefill scores q . [k^C ; k^R] / sqrt(192) per
 head, with 128 content dims, 64 decoupled RoPE dims whose key part all heads
-share, and 128-dim values.  The tensor-core kernel runs (D_qk, D_v) = (192, 128);
-the CUDA-core kernel every other size.  Cases cover tiles plus a ragged tail,
-GQA sharing, both RoPE pairings, no RoPE, the unmasked form, and the full
-DeepSeek-V3-shaped configuration on sampled rows.
+share, and 128-dim values.  (D_qk, D_v) = (192, 128) runs on the CTA-pair
+tensor-core kernel (work items of four 128-row Q tiles), (128, 128) on the
+single-CTA one, every other size on the CUDA-core kernel.  Cases cover tiles plus
+a ragged tail, items whose later tiles lie past the prompt, a single token, GQA
+sharing, both RoPE pairings, no RoPE, the unmasked form, and the full
+DeepSeek-V3-shaped configuration at the edge rows of every Q tile of every head.
 """
 import numpy as np
 import pytest
@@ -31,6 +33,10 @@ def lib():
 CASES = [
     # B, S, n_h, n_kv, D_qk, D_v, rope_base, rope_offset, rope_dims, causal, pairing, dtype
     (1, 300, 4, 4, 192, 128, 1e4, 128, 64, True, "adjacent", "bf16"),    # tensor cores, ragged tail
+    (1, 1, 2, 2, 192, 128, 1e4, 128, 64, True, "adjacent", "bf16"),      # one token: three empty Q tiles
+    (1, 64, 2, 1, 192, 128, 1e4, 128, 64, True, "half", "bf16"),         # one partial tile
+    (1, 513, 3, 3, 192, 128, 1e4, 128, 64, True, "adjacent", "bf16"),    # a second item of one row
+    (2, 1100, 3, 1, 192, 128, 1e4, 128, 64, True, "adjacent", "bf16"),   # several items per pair, MQA
     (2, 257, 4, 2, 192, 128, 1e4, 128, 64, True, "half", "bf16"),        # GQA groups, split halves
     (1, 200, 2, 2, 192, 128, 0.0, 128, 64, True, "adjacent", "bf16"),    # no RoPE
     (1, 190, 2, 1, 192, 128, 1e4, 128, 64, False, "adjacent", "bf16"),   # no mask
@@ -87,38 +93,14 @@ def test_mla_prefill_from_latent_factors(lib):
     assert_parity(out, ref, "bf16", "MLA prefill from factors")
 
 
-def test_mla_prefill_config_full_sampled_rows(lib):
-    cfg = workloads.config("mla_prefill")
-    q, k, v = workloads.mla_prefill_inputs(cfg, seed=0)
-    out, _, lse = lib.prefill_mla(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
-                                  rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
-                                  lse=True)
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out).all())
-    S = cfg["S"]
-    rows = np.array([0, 1, 127, 128, 2047, S - 129, S - 1])
-    for b, h in ((0, 0), (0, 77), (0, 127)):
-        ref, ref_lse = oracle.attention_prefill_rows(q, k, v, b, h, rows, rope_base=cfg["rope_base"],
-                                                     scale=cfg["scale"], rope_offset=cfg["rope_offset"],
-                                                     rope_dims=cfg["rope_dims"])
-        assert_parity(out[b, rows, h], ref, "bf16", f"mla prefill (b={b}, h={h})")
-        assert np.max(np.abs(to_np(lse[b, h, rows]) - ref_lse)) <= BF16_MAX_ABS
+def tile_edge_rows(S, tile=128):
+    """First and last row of every 128-row query tile."""
+    return np.array(sorted({r for t0 in range(0, S, tile) for r in (t0, min(t0 + tile, S) - 1)}))
 
 
-def test_mla_prefill_folded_dealing_over_a_batch(lib):
-    # K/V of 2 x 128 heads x 2048 keys (335 MB) is over twice the L2, so the work items are dealt
-    # as (heavy, light) pairs of one head; every item of both sequences must still be computed once
-    cfg = workloads.config("mla_prefill", B=2, S=2048)
-    q, k, v = workloads.mla_prefill_inputs(cfg, seed=5)
-    out, _, lse = lib.prefill_mla(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
-                                  rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
-                                  lse=True)
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out).all())
+def check_every_slice(q, k, v, cfg, out, lse, what):
     out_c, lse_c = out.cpu(), lse.cpu()
-    # every (b, h) slice at the first and last row of each 128-row query tile: an item dealt to the
-    # wrong head, or a pair of one head computed twice and its partner never, cannot pass
-    rows = np.array(sorted({r for t0 in range(0, cfg["S"], 128) for r in (t0, t0 + 127)}))
+    rows = tile_edge_rows(cfg["S"])
     got, want, worst_lse = [], [], 0.0
     for b in range(cfg["B"]):
         for h in range(cfg["n_h"]):
@@ -129,4 +111,31 @@ def test_mla_prefill_folded_dealing_over_a_batch(lib):
             want.append(ref)
             worst_lse = max(worst_lse, float(np.max(np.abs(to_np(lse_c[b, h, rows]) - ref_lse))))
     assert worst_lse <= BF16_MAX_ABS, f"lse max-abs {worst_lse}"
-    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", "folded mla prefill, every slice")
+    assert_parity(np.concatenate(got), np.concatenate(want), "bf16", what)
+
+
+def test_mla_prefill_config_every_slice(lib):
+    # the benchmark's launch (B=1 S=4096, 128 heads: 1024 items of four Q tiles over the CTA pairs);
+    # every head at the first and last row of each of its Q tiles, so an item computed for the wrong
+    # head or tile, or a pair tile whose CTA 1 half went astray, cannot pass
+    cfg = workloads.config("mla_prefill")
+    q, k, v = workloads.mla_prefill_inputs(cfg, seed=0)
+    out, _, lse = lib.prefill_mla(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
+                                  rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
+                                  lse=True)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    check_every_slice(q, k, v, cfg, out, lse, "mla prefill, every slice")
+
+
+def test_mla_prefill_batch_every_slice(lib):
+    # 2 sequences x 128 heads x 2048 keys (K/V 335 MB, over twice the L2): 512 items dealt over the
+    # pairs in heaviest-first waves; every item of both sequences must be computed once
+    cfg = workloads.config("mla_prefill", B=2, S=2048)
+    q, k, v = workloads.mla_prefill_inputs(cfg, seed=5)
+    out, _, lse = lib.prefill_mla(q.to(DEV), k.to(DEV), v.to(DEV), rope_base=cfg["rope_base"],
+                                  rope_offset=cfg["rope_offset"], rope_dims=cfg["rope_dims"], scale=cfg["scale"],
+                                  lse=True)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    check_every_slice(q, k, v, cfg, out, lse, "mla prefill over a batch, every slice")

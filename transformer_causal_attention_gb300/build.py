@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
-SOURCES = ["prefill_tc.cu", "decode_mla.cu", "decode_tc.cu", "decode_stream.cu", "decode.cu", "prefill_simt.cu", "rope.cu",
-           "api.cu"]
+SOURCES = ["prefill_tc.cu", "prefill_pair.cu", "decode_mla.cu", "decode_tc.cu", "decode_stream.cu", "decode.cu",
+           "prefill_simt.cu", "rope.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

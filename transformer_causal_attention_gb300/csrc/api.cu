@@ -301,8 +301,10 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k
   // It needs every tile pair p to have a partner n_pairs - 1 - p of complementary
   // weight (whole causal prompts, an even number of pairs), and it pays when the
   // K/V of all heads is well beyond L2 - heaviest-first waves touch every head -
-  // and there are several waves of double items.  Measured: the MLA prefill
-  // shape (K/V 2.7x L2) gained 4%, the Llama-3-8B shape (1.1x L2) lost 3%.
+  // and there are several waves of double items.  Measured on prefill_tc.cu: the
+  // MLA prefill shape (K/V 2.7x L2) gained 4%, the Llama-3-8B shape (1.1x L2) lost
+  // 3%.  The CTA-pair kernel of the MLA shape deals heaviest-first only (folded, it
+  // measured 1% slower).
   {
     const long long n_pairs = (S + 255) / 256;
     const long long kv_bytes = static_cast<long long>(B) * n_kv * S * (D_qk + D_v) * static_cast<long long>(esz);
@@ -310,7 +312,16 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k
     pa.fold = (causal && window == 0 && n_pairs % 2 == 0 && kv_bytes > 2LL * dev.l2_bytes &&
                n_double >= 4LL * dev.sms) ? 1 : 0;
   }
-  if (prefill_tc_supported(D_qk, D_v, bf16)) {
+  if (prefill_pair_supported(D_qk, D_v, bf16, window)) {
+    // the MLA prefill shape on CTA pairs: each CTA loads 64-key halves of the K tiles
+    CUtensorMap maps[3];
+    const unsigned long long hs = static_cast<unsigned long long>(D_qk) * 2;
+    if (!make_bshd_map(&maps[0], q, B, S, n_h, D_qk) ||
+        !make_map4(&maps[1], pa.k, D_qk, n_kv, S, B, hs, hs * n_kv, hs * n_kv * S, 64) ||
+        !make_bshd_map(&maps[2], v, B, S, n_kv, D_v))
+      return finish(cudaErrorInvalidValue, launches);
+    e = launch_prefill_pair(pa, rf, maps, st, &launches);
+  } else if (prefill_tc_supported(D_qk, D_v, bf16)) {
     CUtensorMap maps[3];
     if (!make_bshd_map(&maps[0], q, B, S, n_h, D_qk) || !make_bshd_map(&maps[1], pa.k, B, S, n_kv, D_qk) ||
         !make_bshd_map(&maps[2], v, B, S, n_kv, D_v))

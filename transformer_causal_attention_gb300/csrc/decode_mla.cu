@@ -61,6 +61,7 @@
 #include <atomic>
 
 #include "kernels.h"
+#include "pair.cuh"
 
 namespace attn {
 namespace {
@@ -219,32 +220,7 @@ __device__ __forceinline__ bool for_units(int lo, int nr, int r, F&& f) {
   return true;
 }
 
-// ---- pair (cluster) helpers
-__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
-  return a;
-}
-// TMA load whose completion is counted on an mbarrier of either CTA of the pair.
-__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
-                                                 int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair_hint(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
-                                                      int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
+// ---- pair helpers only this kernel uses
 __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
                                             uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
@@ -257,70 +233,6 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on a barrier that the other CTA (or its copies) may complete (acquire at cluster scope).
-__device__ __forceinline__ bool wait_cl(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  if (try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        *w.abort_flag = 1;
-        atomicOr(w.status, STATUS_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  const bool ok = wait_cl(bar, parity, w);
-  return __all_sync(0xffffffffu, ok);
-}
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!try_wait_cluster(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return;
-  }
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// ---- tcgen05 for the pair (every tcgen05 instruction of this kernel uses cta_group::2)
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the barrier at this offset in both CTAs when the pair's MMAs issued so far complete.
-__device__ __forceinline__ void commit_both(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(static_cast<uint16_t>(3))
-      : "memory");
-}
-__device__ __forceinline__ void commit_local(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
 // columns [col, col + 64) of this thread's TMEM lane (taddr) times the per-column factors f[0..63]
 // (shared memory); warp-collective
 __device__ __forceinline__ void scale_cols64(uint32_t taddr, const float* f) {
@@ -575,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     mma_done:
       commit_local(&bars->fin);
-      drain_wait(&bars->fin, 0, a.wait_limit_ns);
+      drain_wait_cl(&bars->fin, 0, a.wait_limit_ns);
     }
     __syncwarp();
   } else if (warp == 2) {

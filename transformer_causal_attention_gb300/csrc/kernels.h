@@ -96,6 +96,11 @@ struct KvAppendArgs {
 cudaError_t launch_prefill_simt(const PrefillArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st,
                                 int* launches);
 bool prefill_tc_supported(int D_qk, int D_v, bool bf16);
+// The MLA prefill shape (q/k head dim 192, v head dim 128, bf16, no window) on the tensor cores
+// of CTA pairs (prefill_pair.cu); maps: Q and V with 128-row boxes, K with 64-row boxes.
+bool prefill_pair_supported(int D_qk, int D_v, bool bf16, int window);
+cudaError_t launch_prefill_pair(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, cudaStream_t st,
+                                int* launches);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps,
                               int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_rope(const RopeArgs& a, const RopeFreq& rope, bool bf16, cudaStream_t st, int* launches);

@@ -28,11 +28,11 @@
 //   CTAs in waves that alternate direction.
 // RoPE: the query tile is rotated in shared memory right after its TMA load
 // (once per item, by the softmax warpgroup, with hardware sin/cos); keys arrive
-// already rotated (written once by the rope pass).  For D_qk = 64 and 128 the Q
-// tiles cycle through three shared-memory slots, so the next item's first tile
-// is in place before the current item ends.
-// Head dims: (64, 64), (128, 128) and the MLA prefill shape D_qk = 192 (128
-// content dims + 64 rotated dims), D_v = 128 ("Transformer 与 LLM" slide 06).
+// already rotated (written once by the rope pass).  The Q tiles cycle through
+// three shared-memory slots, so the next item's first tile is in place before the
+// current item ends.
+// Head dims: (64, 64) and (128, 128); the MLA prefill shape (192, 128) runs on the
+// CTA-pair kernel of prefill_pair.cu.
 // TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1,
 //               [256, 256+D_v) O of tile 0, [256+D_v, 256+2D_v) O of tile 1.
 #include <math.h>
@@ -56,14 +56,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // waits until the pool has the registers, so the split must fit the pool; the
 // launcher checks the compiled register count against it before launching.
 constexpr int kLaunchRegs = 168;
-constexpr int kRegsCtl = 152, kRegsSoftmax = 176;  // 136 / 184 left the issuer of D_qk = 192 spilling
+constexpr int kRegsCtl = 152, kRegsSoftmax = 176;
 constexpr int kRegsNeeded = 4 * 32 * kRegsCtl + 8 * 32 * kRegsSoftmax;
 static_assert(kRegsNeeded <= kThreads * kLaunchRegs, "register split exceeds the launch's pool");
 
 // Head dims DQK (q, k) and DV (v, out).  Every tile is stored as 64-element
 // (128-byte) column blocks of 128 rows with the 128-byte swizzle.  Shared
-// memory holds both Q tiles, kKStages K tiles and kVStages V tiles; with
-// DQK = 192 (the MLA prefill shape) only one V stage fits beside two K stages.
+// memory holds three Q tile slots, kKStages K tiles and kVStages V tiles.
 template <int DQK, int DV>
 struct Cfg {
   static_assert(BM == BN, "Q, K and V tiles share one row count");
@@ -72,11 +71,12 @@ struct Cfg {
   static constexpr int kQKTileBytes = BM * DQK * 2;
   static constexpr int kVTileBytes = BN * DV * 2;
   static constexpr int kBlockBytes = BM * 128;    // one column block of a tile
+  static_assert((DQK == 64 && DV == 64) || (DQK == 128 && DV == 128), "head dims");
   static constexpr int kKStages = DQK == 64 ? 3 : 2;
-  static constexpr int kVStages = DQK == 64 ? 3 : (DQK == 128 ? 2 : 1);
-  // Q tile slots: a third slot (D_qk = 64 and 128, where it fits) lets the next
-  // item's first Q tile load while the current item still runs
-  static constexpr int kQSlots = DQK == 192 ? 2 : 3;
+  static constexpr int kVStages = DQK == 64 ? 3 : 2;
+  // Q tile slots: the third lets the next item's first Q tile load while the
+  // current item still runs
+  static constexpr int kQSlots = 3;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQSlots * kQKTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kQKTileBytes;
@@ -466,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the softmax hands over P in two halves of 64 keys: the first half's P V runs
                 // while it computes the second half
                 if (!mbar_wait(&bars->p_half[0], pph0, wc)) goto mma_done;
-                if (C::kVStages == 1 && !mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
                 tc_fence_after();
                 issue_pv_half(0, vst, true, 0);
                 if (!mbar_wait(&bars->p_full[0], pph0, wc)) goto mma_done;
@@ -488,9 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t kst_n = kst + 1, kph_n = kph;
                 if (kst_n == static_cast<uint32_t>(C::kKStages)) { kst_n = 0; kph_n ^= 1; }
                 if (v + 1 < ve) {
-                  // (with one V stage the next V tile only starts loading now: it is waited for at
-                  // the top of the next iteration instead)
-                  if (C::kVStages > 1 && !mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
+                  if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
                   if (!mbar_wait(&bars->k_full[kst_n], kph_n, wc)) goto mma_done;
                 }
                 issue_qk_part(1, qs1, kst, 1);
@@ -564,12 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sph = 0;
     uint32_t it = 0;
     // Q tile t of the k-th item: wait for its load, rotate this thread's row, hand it
-    // to the MMA issuer.  With kEarlyQ the tile is released as soon as its last Q K has
-    // completed, and the next item's tile is prepared before this item's epilogue, so
-    // that the new item's first Q K overlaps that epilogue (Llama-3-8B prefill 1.92 ->
-    // 1.91 ms).  The MLA shape measured 2% slower that way and keeps the plain order:
-    // epilogue, release, then the next item's Q.
-    constexpr bool kEarlyQ = DQK != 192;
+    // to the MMA issuer.  The tile is released as soon as its last Q K has completed,
+    // and the next item's tile is prepared before this item's epilogue, so that the new
+    // item's first Q K overlaps that epilogue (Llama-3-8B prefill 1.92 -> 1.91 ms).
     uint32_t cur_qs = static_cast<uint32_t>(t), cur_qp = 0;  // this tile's Q slot and parity in the current item
     auto prepare_q = [&](uint32_t qs, uint32_t qp, int item_idx) -> bool {
       if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
@@ -583,9 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     int idx = item_at<FOLD>(0);
-    if (kEarlyQ && idx < n_items && !prepare_q(cur_qs, cur_qp, idx)) idx = n_items;
+    if (idx < n_items && !prepare_q(cur_qs, cur_qp, idx)) idx = n_items;
     while (idx < n_items) {
-      if (!kEarlyQ && !prepare_q(cur_qs, cur_qp, idx)) break;
       const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
       const int qt = itm.qt0 + t;
       const TileRange rng = t ? itm.r1 : itm.r0;
@@ -601,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1;
         tc_fence_after();
         // the last Q K of this tile has completed: the producer may load the next item's Q
-        if (kEarlyQ && i == n_t - 1) mbar_arrive(&bars->q_empty[cur_qs]);
+        if (i == n_t - 1) mbar_arrive(&bars->q_empty[cur_qs]);
         uint32_t sr[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
@@ -707,12 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int next_idx = item_at<FOLD>(it + 1);
       uint32_t nxt_qs = cur_qs, nxt_qp = cur_qp;
       q_advance(nxt_qs, nxt_qp, 2);
-      if (kEarlyQ && next_idx < n_items && !prepare_q(nxt_qs, nxt_qp, next_idx)) break;
+      if (next_idx < n_items && !prepare_q(nxt_qs, nxt_qp, next_idx)) break;
 
       // epilogue: O / l -> out (rows past S are computed but not stored)
       if (!warp_wait(&bars->o_done[t], it & 1, wc)) break;
       tc_fence_after();
-      if (!kEarlyQ) mbar_arrive(&bars->q_empty[cur_qs]);  // every MMA reading Q_t has completed
       const float inv_l = 1.f / l_run;
       const bool store = m < a.S;
       __nv_bfloat16* orow_g = static_cast<__nv_bfloat16*>(a.out) +
@@ -756,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 namespace {
-// Per head-dim pair, one bit per device that has been prepared.
-std::atomic<unsigned> g_ready[5];
+// Per instantiation, one bit per device that has been prepared.
+std::atomic<unsigned> g_ready[3];
 
 // Opt in to the kernel's shared memory and check, once per process and device,
 // that the compiled kernel holds enough registers per thread for its register
@@ -790,7 +782,7 @@ cudaError_t launch(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap
 }  // namespace
 
 bool prefill_tc_supported(int D_qk, int D_v, bool bf16) {
-  return bf16 && ((D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128) || (D_qk == 192 && D_v == 128));
+  return bf16 && ((D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128));
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
@@ -804,11 +796,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const 
   if (a.D == 64)
     e = launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
   else if (a.D == 128)
-    e = a.fold ? launch<128, 128, true>(a, rope, maps, grid, st, &g_ready[3])
+    e = a.fold ? launch<128, 128, true>(a, rope, maps, grid, st, &g_ready[2])
                : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
   else
-    e = a.fold ? launch<192, 128, true>(a, rope, maps, grid, st, &g_ready[4])
-               : launch<192, 128>(a, rope, maps, grid, st, &g_ready[2]);
+    e = cudaErrorInvalidValue;
   *launches += 1;
   return e;
 }
