@@ -16,7 +16,7 @@
 // So each CTA holds half of every K and V tile: with 192-dim keys the shared memory then
 // takes three K and V stages next to two Q tiles, where prefill_tc.cu's <192, 128> layout
 // has room for one V stage.  The softmax is that of prefill_tc.cu, one thread per query row
-// of the CTA's own tile, P handed to the issuer in two halves of 64 keys; a pair tile's key
+// of the CTA's own tile, P handed to the issuer once per key tile; a pair tile's key
 // range is the one of its later (CTA 1) tile, so CTA 0 also computes the one key tile after
 // its own diagonal, entirely masked.
 // Hand-offs to the issuer from the odd CTA's warps are arrivals on the even CTA's barriers
@@ -79,7 +79,7 @@ constexpr uint32_t kWarpArrivals = 8;  // softmax warps of a pair tile in both C
 
 struct Bars {
   uint64_t q_full[kQSlots], q_ready[kQSlots], q_empty[kQSlots];
-  uint64_t s_full[2], p_half[2], p_full[2], o_done[2], o_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t fin;
   uint32_t tmem_base;
@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_half[t], kWarpArrivals);
       mbar_init(&bars->p_full[t], kWarpArrivals);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_empty[t], kWarpArrivals);
@@ -309,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer (CTA 0)
       // Per loaded key tile j, for each pair tile t that needs it: P_t V(j) then Q_t K(j + 1), with
-      // the decision-free steady loop and P handed over in halves of 64 keys, as in prefill_tc.cu.
+      // the decision-free steady loop, as in prefill_tc.cu.
       if (lane == 0 && r == 0) {
         const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem(0)), 16, 1024);
         const uint64_t k_desc0 = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);
@@ -328,17 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                      b0 + (((kk >> 2) * kKHalfBlock + (kk & 3) * 32) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
         };
         auto issue_qk = [&](int t, uint32_t qslot, uint32_t stage) { issue_qk_part(t, qslot, stage, -1); };
-        // P_t V over the keys [64 half, 64 half + 64) of the tile
-        auto issue_pv_half = [&](int t, uint32_t stage, bool accumulate, int half) {
+        // P_t V over the tile's 128 keys (P of keys [16 kk, 16 kk + 16) in TMEM columns [8 kk, 8 kk + 8)
+        // of the tile's S columns)
+        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
           const uint64_t b0 = v_desc0 + ((stage * kVHalfBytes) >> 4);
 #pragma unroll
-          for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+          for (int kk = 0; kk < BN / 16; ++kk)
             mma_pair_ts(tmem + kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV,
                         (accumulate || kk > 0) ? 1u : 0u);
-        };
-        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
-          issue_pv_half(t, stage, accumulate, 0);
-          issue_pv_half(t, stage, accumulate, 1);
         };
         for (int idx = item_at(it); idx < n_items; idx = item_at(++it)) {
           const Item itm = decode_item(idx, a, n_quads, n_kt);
@@ -361,22 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!wait_cl(&bars->v_full[vst], vph, wc)) goto mma_done;
               if (!wait_cl(&bars->k_full[kst], kph, wc)) goto mma_done;
               for (; v < ve; ++v) {
-                if (!wait_cl(&bars->p_half[0], pph0, wc)) goto mma_done;
-                tc_fence_after();
-                issue_pv_half(0, vst, true, 0);
                 if (!wait_cl(&bars->p_full[0], pph0, wc)) goto mma_done;
                 pph0 ^= 1;
                 tc_fence_after();
-                issue_pv_half(0, vst, true, 1);
+                issue_pv(0, vst, true);
                 issue_qk(0, qs0, kst);
                 commit_both(&bars->s_full[0]);
-                if (!wait_cl(&bars->p_half[1], pph1, wc)) goto mma_done;
-                tc_fence_after();
-                issue_pv_half(1, vst, true, 0);
                 if (!wait_cl(&bars->p_full[1], pph1, wc)) goto mma_done;
                 pph1 ^= 1;
                 tc_fence_after();
-                issue_pv_half(1, vst, true, 1);
+                issue_pv(1, vst, true);
                 commit_both(&bars->v_empty[vst]);
                 if (++vst == kVStages) { vst = 0; vph ^= 1; }
                 issue_qk_part(1, qs1, kst, 0);
@@ -402,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const TileRange& rg = t ? itm.r1 : itm.r0;
               const bool pv = rg.has(j), qk = next && rg.has(jn);
               if (pv) {
-                if (!wait_cl(&bars->p_half[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (!wait_cl(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (t) pph1 ^= 1; else pph0 ^= 1;
                 if (!(t ? pv_seen1 : pv_seen0) && !wait_cl(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
@@ -451,7 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + kOCol0 + (t ? DV : 0);
     // the barriers the issuer waits on (in CTA 0): one arrival per warp
     const uint32_t q_ready0 = cluster_addr(&bars->q_ready[0], 0);
-    const uint32_t p_half0 = cluster_addr(&bars->p_half[t], 0);
     const uint32_t p_full0 = cluster_addr(&bars->p_full[t], 0);
     const uint32_t o_empty0 = cluster_addr(&bars->o_empty[t], 0);
     auto warp_arrive = [&](uint32_t bar_cluster) {
@@ -554,9 +542,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_addr + c * 32, orow);
           }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(p_half0);
 #pragma unroll
         for (int c = BN / 4; c < BN / 2; ++c) {
           const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);

@@ -92,7 +92,7 @@ struct Cfg {
 
 struct Bars {
   uint64_t q_full[3], q_ready[3], q_empty[3];  // per Q slot
-  uint64_t s_full[2], p_half[2], p_full[2], o_done[2], o_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];  // up to 3 stages
   uint64_t fin;
   uint32_t tmem_base;
@@ -284,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_half[t], 128);
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_empty[t], 128);
@@ -415,20 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         auto issue_qk = [&](int t, uint32_t qslot, uint32_t stage) { issue_qk_part(t, qslot, stage, -1); };
-        // P_t V over the keys [64 half, 64 half + 64) of the tile (P of those keys sits in TMEM
-        // columns [32 half, 32 half + 32) of the tile's S columns, two bf16 per column)
-        auto issue_pv_half = [&](int t, uint32_t stage, bool accumulate, int half) {
+        // P_t V over the tile's 128 keys (P of keys [16 kk, 16 kk + 16) sits in TMEM columns
+        // [8 kk, 8 kk + 8) of the tile's S columns, two bf16 per column)
+        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
           const uint64_t b0 = v_desc0 + ((stage * C::kVTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+          for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
-        auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
-          issue_pv_half(t, stage, accumulate, 0);
-          issue_pv_half(t, stage, accumulate, 1);
-        };
-        static_assert(BN == 128, "P V is issued in two halves of 64 keys");
         for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
           const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
@@ -463,24 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!mbar_wait(&bars->v_full[vst], vph, wc)) goto mma_done;
               if (!mbar_wait(&bars->k_full[kst], kph, wc)) goto mma_done;
               for (; v < ve; ++v) {
-                // the softmax hands over P in two halves of 64 keys: the first half's P V runs
-                // while it computes the second half
-                if (!mbar_wait(&bars->p_half[0], pph0, wc)) goto mma_done;
-                tc_fence_after();
-                issue_pv_half(0, vst, true, 0);
+                // P of a tile is handed over whole: the softmax finishes it before the issuer
+                // asks (a trace of this loop showed every P wait returning at once), so a split
+                // hand-off would only add waits and fences between the MMA bursts
                 if (!mbar_wait(&bars->p_full[0], pph0, wc)) goto mma_done;
                 pph0 ^= 1;
                 tc_fence_after();
-                issue_pv_half(0, vst, true, 1);
+                issue_pv(0, vst, true);
                 issue_qk(0, qs0, kst);
                 mma_commit(&bars->s_full[0]);
-                if (!mbar_wait(&bars->p_half[1], pph1, wc)) goto mma_done;
-                tc_fence_after();
-                issue_pv_half(1, vst, true, 0);
                 if (!mbar_wait(&bars->p_full[1], pph1, wc)) goto mma_done;
                 pph1 ^= 1;
                 tc_fence_after();
-                issue_pv_half(1, vst, true, 1);
+                issue_pv(1, vst, true);
                 mma_commit(&bars->v_empty[vst]);
                 if (++vst == C::kVStages) { vst = 0; vph ^= 1; }
                 issue_qk_part(1, qs1, kst, 0);
@@ -506,7 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const TileRange& r = t ? itm.r1 : itm.r0;
               const bool pv = r.has(j), qk = next && r.has(jn);
               if (pv) {
-                if (!mbar_wait(&bars->p_half[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (!mbar_wait(&bars->p_full[t], t ? pph1 : pph0, wc)) goto mma_done;
                 if (t) pph1 ^= 1; else pph0 ^= 1;
                 if (!(t ? pv_seen1 : pv_seen0) && !mbar_wait(&bars->o_empty[t], (it & 1) ^ 1, wc)) goto mma_done;
@@ -647,8 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // p = 2^(s * scale*log2e - m), two columns per packed fp32x2 FMA; the row
         // sum runs in 4 independent packed accumulators.  P goes back to TMEM in two
-        // halves of 64 keys, each announced on its own barrier, so that the MMA issuer
-        // runs the first half's P V while the second half is computed.
+        // stores of 64 keys (the first drains while the second half is computed) and is
+        // announced once.
         uint32_t pr[BN / 2];
         const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
         // a row whose tiles so far held no visible key keeps m = -inf: its
@@ -679,9 +667,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_addr + c * 32, orow);
           }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_half[t]);
 #pragma unroll
         for (int c = BN / 4; c < BN / 2; ++c) {
           const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);
