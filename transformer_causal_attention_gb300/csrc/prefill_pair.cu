@@ -567,23 +567,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const bool store = m < a.S;
-      __nv_bfloat16* orow_g = static_cast<__nv_bfloat16*>(a.out) +
-                              ((static_cast<long long>(itm.b) * a.S + m) * a.n_h + itm.h) * DV;
+      // Each lane of a group of four stores 16-byte pieces of the group's four rows, so that one
+      // store instruction writes 64 contiguous bytes of each of eight rows (a row's own lane would
+      // write 16 bytes of each of 32 rows 8 KB apart)
+      const int lj = lane & 3;
+      const int m_base = m - lj;  // first row of this lane's group
+      __nv_bfloat16* const og = static_cast<__nv_bfloat16*>(a.out) +
+                                ((static_cast<long long>(itm.b) * a.S + m_base) * a.n_h + itm.h) * DV + lj * 8;
+      const long long row_step = static_cast<long long>(a.n_h) * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t orow[32];
         tmem_ld32(o_addr + c * 32, orow);
         tmem_wait_ld();
-        if (store) {
-          uint32_t packed[16];
+        uint4 pc[4];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            packed[e] = pack_bf16x2(__uint_as_float(orow[2 * e]) * inv_l, __uint_as_float(orow[2 * e + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        for (int e = 0; e < 4; ++e)
+          pc[e] = make_uint4(pack_bf16x2(__uint_as_float(orow[8 * e]) * inv_l, __uint_as_float(orow[8 * e + 1]) * inv_l),
+                             pack_bf16x2(__uint_as_float(orow[8 * e + 2]) * inv_l, __uint_as_float(orow[8 * e + 3]) * inv_l),
+                             pack_bf16x2(__uint_as_float(orow[8 * e + 4]) * inv_l, __uint_as_float(orow[8 * e + 5]) * inv_l),
+                             pack_bf16x2(__uint_as_float(orow[8 * e + 6]) * inv_l, __uint_as_float(orow[8 * e + 7]) * inv_l));
+        // 4 x 4 transpose of the pieces within the group (two exchange rounds): afterwards pc[k] is
+        // piece lj of row m_base + k
+        {
+          const bool b1 = (lj & 2) != 0;
+          uint4 s0 = b1 ? pc[0] : pc[2], s1 = b1 ? pc[1] : pc[3];
+          uint4 r0 = shfl_xor_u4(s0, 2), r1 = shfl_xor_u4(s1, 2);
+          if (b1) { pc[0] = r0; pc[1] = r1; } else { pc[2] = r0; pc[3] = r1; }
+          const bool b0 = (lj & 1) != 0;
+          s0 = b0 ? pc[0] : pc[1];
+          s1 = b0 ? pc[2] : pc[3];
+          r0 = shfl_xor_u4(s0, 1);
+          r1 = shfl_xor_u4(s1, 1);
+          if (b0) { pc[0] = r0; pc[2] = r1; } else { pc[1] = r0; pc[3] = r1; }
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (m_base + k < a.S) *reinterpret_cast<uint4*>(og + k * row_step + c * 32) = pc[k];
       }
       tc_fence_before();
       warp_arrive(o_empty0);
