@@ -312,6 +312,8 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out, void* k
     pa.fold = (causal && window == 0 && n_pairs % 2 == 0 && kv_bytes > 2LL * dev.l2_bytes &&
                n_double >= 4LL * dev.sms) ? 1 : 0;
   }
+  // GQA: a work item takes one Q tile of two heads that read the same K/V head (prefill_tc.cu)
+  pa.head_pairs = (n_h / n_kv) % 2 == 0 ? 1 : 0;
   if (prefill_pair_supported(D_qk, D_v, bf16, window)) {
     // the MLA prefill shape on CTA pairs: each CTA loads 64-key halves of the K tiles
     CUtensorMap maps[3];
@@ -358,6 +360,7 @@ int attn_prefill_chunk(const void* q, const void* kcache, const void* vcache, vo
   const int S_k = q_offset + S_q;
   PrefillArgs pa{q, kcache, vcache, out, lse, B, S_q, n_h, n_kv, D_h, sc * kLog2e, causal, dev.status,
                  g_wait_limit_ns.load(), S_k, q_offset, max_len, 0, 0, D_h, 0};
+  pa.head_pairs = (n_h / n_kv) % 2 == 0 ? 1 : 0;  // GQA: one Q tile of two heads per work item
   const RopeFreq rf = make_rope(rope_base, D_h, half);
   int launches = 0;
   cudaError_t e;

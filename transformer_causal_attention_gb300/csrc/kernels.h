@@ -29,6 +29,7 @@ struct PrefillArgs {
   int D_v;           // head dim of v and out
   int rope_offset;   // first rotated dim of q and k (the span holds 2 * n_pairs dims)
   int fold;          // 1: deal work items as (heavy, light) pairs of one head, head after head
+  int head_pairs;    // 1: a work item is one Q tile of two query heads of a K/V group (n_h / n_kv even)
 };
 
 struct DecodeArgs {

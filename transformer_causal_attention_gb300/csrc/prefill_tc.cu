@@ -112,6 +112,8 @@ struct TileRange {
 
 struct Item {
   int b, h, g, qt0;
+  int dq, dh;        // Q tile t is tile qt0 + t dq of head h + t dh (adjacent tiles of one head, or one tile
+                     // of two heads that share a K/V head)
   TileRange r0, r1;  // the two Q tiles
   int ns_u, n_load;  // loaded tiles: [0, ns_u) then [r0.jl, r1.jh]
   __device__ __forceinline__ int load_at(int v) const { return v < ns_u ? v : r0.jl + v - ns_u; }
@@ -138,6 +140,11 @@ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, in
   return r;
 }
 
+// Dealing of work items (a template parameter of the kernel):
+constexpr int kDealTiles = 0;      // two adjacent Q tiles of one (batch, head), heaviest-first waves
+constexpr int kDealTilesFold = 1;  // the same items, folded (below)
+constexpr int kDealHeads = 2;      // one Q tile of two heads of a K/V group, heaviest-first waves
+
 // Index of this CTA's k-th work item.  Items are sorted heaviest-first and dealt out in waves
 // of gridDim.x, every other wave in reverse CTA order, so that no CTA takes the heaviest item of
 // every wave (with one direction only, the busiest CTA of the Llama-3-8B prefill would carry
@@ -146,20 +153,47 @@ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, in
 // one (batch, head), heavy one first, which together always hold the same number of key
 // tiles; double items go out head after head, so the CTAs running at one time share few K/V
 // heads and their key tiles are re-read from L2 rather than HBM.
+// With GQA, an item can instead take one Q tile of two query heads that read the same K/V head:
+// both tiles then have the same key tiles, so neither waits at the item's end for the other's
+// one extra key tile, and both warpgroups reach the boundary together.
 // The dealing is a template parameter: a run-time switch here cost the Llama-3-8B
 // prefill 2.7% (register spills in the item loops).
-template <bool FOLD>
+template <int DEAL>
 __device__ __forceinline__ int item_at(uint32_t k) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  if constexpr (FOLD) return 2 * (static_cast<int>(k >> 1) * g + c) + static_cast<int>(k & 1u);
+  if constexpr (DEAL == kDealTilesFold) return 2 * (static_cast<int>(k >> 1) * g + c) + static_cast<int>(k & 1u);
   return static_cast<int>(k) * g + ((k & 1u) ? g - 1 - c : c);
 }
 
-template <bool FOLD>
+// Items per CTA-independent unit count: tile pairs per (batch, head), or Q tiles per head.
+template <int DEAL>
+__host__ __device__ __forceinline__ long long n_work_items(int B, int n_h, int n_qt) {
+  if constexpr (DEAL == kDealHeads) return static_cast<long long>(B) * (n_h / 2) * n_qt;
+  return static_cast<long long>(B) * n_h * ((n_qt + 1) / 2);
+}
+
+template <int DEAL>
 __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n_pairs_q, int n_kt) {
   Item it;
+  if constexpr (DEAL == kDealHeads) {
+    const int n_qt = (a.S + BM - 1) / BM;
+    const int bhp_count = a.B * (a.n_h / 2);
+    const int q = n_qt - 1 - idx / bhp_count;  // heaviest (latest) Q tiles first
+    const int bhp = idx % bhp_count;
+    it.b = bhp / (a.n_h / 2);
+    it.h = 2 * (bhp % (a.n_h / 2));
+    it.g = it.h / (a.n_h / a.n_kv);
+    it.qt0 = q;
+    it.dq = 0;
+    it.dh = 1;
+    it.r0 = tile_range(q, a, n_kt);
+    it.r1 = it.r0;
+    it.ns_u = it.r0.ns;
+    it.n_load = it.ns_u + it.r1.jh - it.r0.jl + 1;
+    return it;
+  }
   int p, bh;
-  if constexpr (FOLD) {  // n_pairs_q is even
+  if constexpr (DEAL == kDealTilesFold) {  // n_pairs_q is even
     const unsigned half = static_cast<unsigned>(n_pairs_q) >> 1, d = static_cast<unsigned>(idx) >> 1;
     bh = static_cast<int>(d / half);
     const int j = static_cast<int>(d - static_cast<unsigned>(bh) * half);
@@ -173,6 +207,8 @@ __device__ __forceinline__ Item decode_item(int idx, const PrefillArgs& a, int n
   it.h = bh % a.n_h;
   it.g = it.h / (a.n_h / a.n_kv);
   it.qt0 = 2 * p;
+  it.dq = 1;
+  it.dh = 0;
   it.r0 = tile_range(it.qt0, a, n_kt);
   it.r1 = tile_range(it.qt0 + 1, a, n_kt);
   // tile 1's window starts no earlier and ends no earlier than tile 0's, and its
@@ -253,7 +289,7 @@ __device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope
   }
 }
 
-template <int DQK, int DV, bool FOLD>
+template <int DQK, int DV, int DEAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -274,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_qt = (a.S + BM - 1) / BM;
   const int n_kt = (a.S_k + BN - 1) / BN;
   const int n_pairs_q = (n_qt + 1) / 2;
-  const int n_items = a.B * a.n_h * n_pairs_q;
+  const int n_items = static_cast<int>(n_work_items<DEAL>(a.B, a.n_h, n_qt));
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < C::kQSlots; ++q) {
@@ -352,15 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
         uint32_t q_armed = 0, q_last = 0, it = 0;  // bit q: slot q loaded / parity of its last load
         uint32_t qs = 0, qp = 0;                    // slot and parity of position 2 it + t
-        for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
-          const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
+        for (int idx = item_at<DEAL>(it); idx < n_items; idx = item_at<DEAL>(++it)) {
+          const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
           if (is_v) {
             for (int t = 0; t < 2; ++t, q_advance(qs, qp, 1)) {
               if (!mbar_wait(&bars->q_empty[qs], qp ^ 1, wc)) goto load_done;
               mbar_arrive_expect_tx(&bars->q_full[qs], C::kQKTileBytes);
               for (int db = 0; db < C::kQBlocks; ++db)
-                tma_load_4d(q_smem(qs) + db * C::kBlockBytes, &tm_q, &bars->q_full[qs], db * 64, itm.h,
-                            (itm.qt0 + t) * BM, itm.b);
+                tma_load_4d(q_smem(qs) + db * C::kBlockBytes, &tm_q, &bars->q_full[qs], db * 64, itm.h + t * itm.dh,
+                            (itm.qt0 + t * itm.dq) * BM, itm.b);
               q_armed |= 1u << qs;
               q_last = (q_last & ~(1u << qs)) | (qp << qs);
             }
@@ -423,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int idx = item_at<FOLD>(it); idx < n_items; idx = item_at<FOLD>(++it)) {
-          const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
+        for (int idx = item_at<DEAL>(it); idx < n_items; idx = item_at<DEAL>(++it)) {
+          const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
           uint32_t qs1 = qs0, qp1 = qp0;
           q_advance(qs1, qp1, 1);
@@ -556,19 +592,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prepare_q = [&](uint32_t qs, uint32_t qp, int item_idx) -> bool {
       if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
       if (f.n_pairs) {
-        const Item nx = decode_item<FOLD>(item_idx, a, n_pairs_q, n_kt);
-        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t) * BM + r, a.rope_offset, f.n_pairs,
+        const Item nx = decode_item<DEAL>(item_idx, a, n_pairs_q, n_kt);
+        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t * nx.dq) * BM + r, a.rope_offset, f.n_pairs,
                           f.half != 0, f_hi, f_lo);
         fence_proxy_async_smem();
       }
       mbar_arrive(&bars->q_ready[qs]);
       return true;
     };
-    int idx = item_at<FOLD>(0);
+    int idx = item_at<DEAL>(0);
     if (idx < n_items && !prepare_q(cur_qs, cur_qp, idx)) idx = n_items;
     while (idx < n_items) {
-      const Item itm = decode_item<FOLD>(idx, a, n_pairs_q, n_kt);
-      const int qt = itm.qt0 + t;
+      const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
+      const int qt = itm.qt0 + t * itm.dq;
+      const int hd = itm.h + t * itm.dh;  // this tile's query head
       const TileRange rng = t ? itm.r1 : itm.r0;
       const int n_t = rng.count();
       const int m = qt * BM + r;  // query row
@@ -682,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->p_full[t]);
       }
       if (!ok) break;
-      const int next_idx = item_at<FOLD>(it + 1);
+      const int next_idx = item_at<DEAL>(it + 1);
       uint32_t nxt_qs = cur_qs, nxt_qp = cur_qp;
       q_advance(nxt_qs, nxt_qp, 2);
       if (next_idx < n_items && !prepare_q(nxt_qs, nxt_qp, next_idx)) break;
@@ -698,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lj = lane & 3;
       const int m_base = m - lj;  // first row of this lane's group
       __nv_bfloat16* const og = static_cast<__nv_bfloat16*>(a.out) +
-                                ((static_cast<long long>(itm.b) * a.S + m_base) * a.n_h + itm.h) * DV + lj * 8;
+                                ((static_cast<long long>(itm.b) * a.S + m_base) * a.n_h + hd) * DV + lj * 8;
       const long long row_step = static_cast<long long>(a.n_h) * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
@@ -733,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->o_empty[t]);
       if (store && a.lse != nullptr)
-        a.lse[(static_cast<long long>(itm.b) * a.n_h + itm.h) * a.S + m] =
+        a.lse[(static_cast<long long>(itm.b) * a.n_h + hd) * a.S + m] =
             (m_run + log2f(l_run)) * 0.69314718055994530942f;
       idx = next_idx;
       cur_qs = nxt_qs;
@@ -754,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 // Per instantiation, one bit per device that has been prepared.
-std::atomic<unsigned> g_ready[3];
+std::atomic<unsigned> g_ready[5];
 
 // Opt in to the kernel's shared memory and check, once per process and device,
 // that the compiled kernel holds enough registers per thread for its register
@@ -775,10 +812,10 @@ cudaError_t prepare(K kernel, int smem_bytes, std::atomic<unsigned>* ready) {
   return cudaSuccess;
 }
 
-template <int DQK, int DV, bool FOLD = false>
+template <int DQK, int DV, int DEAL = kDealTiles>
 cudaError_t launch(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int grid, cudaStream_t st,
                    std::atomic<unsigned>* ready) {
-  auto k = prefill_tc_kernel<DQK, DV, FOLD>;
+  auto k = prefill_tc_kernel<DQK, DV, DEAL>;
   const cudaError_t e = prepare(k, Cfg<DQK, DV>::kSmemBytes, ready);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, Cfg<DQK, DV>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
@@ -793,16 +830,20 @@ bool prefill_tc_supported(int D_qk, int D_v, bool bf16) {
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int num_sms,
                               cudaStream_t st, int* launches) {
   const int n_qt = (a.S + BM - 1) / BM;
-  const long long n_items = static_cast<long long>(a.B) * a.n_h * ((n_qt + 1) / 2);
+  const bool heads = a.head_pairs && !a.fold && (a.n_h / a.n_kv) % 2 == 0;
+  const long long n_items =
+      heads ? n_work_items<kDealHeads>(a.B, a.n_h, n_qt) : n_work_items<kDealTiles>(a.B, a.n_h, n_qt);
   const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
   cudaError_t e;
   // folded dealing is built for the two larger head dims (D = 64 prompts whose K/V
   // pass twice the L2 take the plain dealing)
   if (a.D == 64)
-    e = launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
+    e = heads ? launch<64, 64, kDealHeads>(a, rope, maps, grid, st, &g_ready[3])
+              : launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
   else if (a.D == 128)
-    e = a.fold ? launch<128, 128, true>(a, rope, maps, grid, st, &g_ready[2])
-               : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
+    e = a.fold ? launch<128, 128, kDealTilesFold>(a, rope, maps, grid, st, &g_ready[2])
+               : heads ? launch<128, 128, kDealHeads>(a, rope, maps, grid, st, &g_ready[4])
+                       : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
   else
     e = cudaErrorInvalidValue;
   *launches += 1;
