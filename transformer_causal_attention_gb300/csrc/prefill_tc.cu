@@ -289,6 +289,59 @@ __device__ __noinline__ void rotate_q_row(uint8_t* row, int r, int pos, int rope
   }
 }
 
+// The same rotation for row r of two Q tiles at the same positions (a GQA work item's two
+// heads), over loop iterations [i_lo, i_hi): each sin/cos serves both rows.  The two softmax
+// warpgroups split the iterations between them, so each computes half the angles.
+template <int DQK>
+__device__ __noinline__ void rotate_q_rows2(uint8_t* row_a, uint8_t* row_b, int r, int pos, int rope_offset,
+                                          int n_pairs, bool half, const float* f_hi, const float* f_lo, int i_lo,
+                                          int i_hi) {
+  constexpr int kBlockBytes = BM * 128;
+  const int sw = r & 7;
+  auto off = [&](int c) -> int { return (c >> 3) * kBlockBytes + (((c & 7) ^ sw) << 4); };
+  const int c0 = rope_offset / 8;
+  if (half) {
+    const int hc = n_pairs / 8;
+#pragma unroll 1
+    for (int i = i_lo; i < i_hi; ++i) {
+      const int o0 = off(c0 + i), o1 = off(c0 + i + hc);
+      float a0[8], a1[8], b0[8], b1[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_a + o0), a0);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_a + o1), a1);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_b + o0), b0);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_b + o1), b1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float sn, cs;
+        rope_sincos_fast(pos, f_hi[i * 8 + e], f_lo[i * 8 + e], &sn, &cs);
+        rotate_pair(a0[e], a1[e], sn, cs);
+        rotate_pair(b0[e], b1[e], sn, cs);
+      }
+      *reinterpret_cast<uint4*>(row_a + o0) = f32_to_bf16x8(a0);
+      *reinterpret_cast<uint4*>(row_a + o1) = f32_to_bf16x8(a1);
+      *reinterpret_cast<uint4*>(row_b + o0) = f32_to_bf16x8(b0);
+      *reinterpret_cast<uint4*>(row_b + o1) = f32_to_bf16x8(b1);
+    }
+  } else {
+#pragma unroll 1
+    for (int i = i_lo; i < i_hi; ++i) {
+      const int o = off(c0 + i);
+      float a[8], b[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_a + o), a);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_b + o), b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float sn, cs;
+        rope_sincos_fast(pos, f_hi[i * 4 + e], f_lo[i * 4 + e], &sn, &cs);
+        rotate_pair(a[2 * e], a[2 * e + 1], sn, cs);
+        rotate_pair(b[2 * e], b[2 * e + 1], sn, cs);
+      }
+      *reinterpret_cast<uint4*>(row_a + o) = f32_to_bf16x8(a);
+      *reinterpret_cast<uint4*>(row_b + o) = f32_to_bf16x8(b);
+    }
+  }
+}
+
 template <int DQK, int DV, int DEAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RopeFreq f,
@@ -315,7 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int q = 0; q < C::kQSlots; ++q) {
       mbar_init(&bars->q_full[q], 1);
-      mbar_init(&bars->q_ready[q], 128);  // the softmax warpgroup of the tile in the slot
+      // the softmax warpgroup of the tile in the slot; with the GQA dealing both warpgroups,
+      // which rotate the item's two tiles together
+      mbar_init(&bars->q_ready[q], DEAL == kDealHeads ? 256 : 128);
       mbar_init(&bars->q_empty[q], 128);
     }
     for (int t = 0; t < 2; ++t) {
@@ -590,14 +645,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // item's first Q K overlaps that epilogue (Llama-3-8B prefill 1.92 -> 1.91 ms).
     uint32_t cur_qs = static_cast<uint32_t>(t), cur_qp = 0;  // this tile's Q slot and parity in the current item
     auto prepare_q = [&](uint32_t qs, uint32_t qp, int item_idx) -> bool {
-      if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
-      if (f.n_pairs) {
-        const Item nx = decode_item<DEAL>(item_idx, a, n_pairs_q, n_kt);
-        rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t * nx.dq) * BM + r, a.rope_offset, f.n_pairs,
-                          f.half != 0, f_hi, f_lo);
-        fence_proxy_async_smem();
+      if constexpr (DEAL == kDealHeads) {
+        // the item's two tiles sit in slot qs - t and qs - t + 1 (mod 3) and share their rows'
+        // positions: warpgroup t rotates iterations [t n / 2, (t + 1) n / 2) of row r of both
+        const uint32_t qa = t ? (qs == 0 ? 2u : qs - 1) : qs, qb = t ? qs : (qs == 2 ? 0u : qs + 1);
+        const uint32_t pa = t ? (qs == 0 ? qp ^ 1u : qp) : qp, pb = t ? qp : (qs == 2 ? qp ^ 1u : qp);
+        if (!warp_wait(&bars->q_full[qa], pa, wc)) return false;
+        if (!warp_wait(&bars->q_full[qb], pb, wc)) return false;
+        if (f.n_pairs) {
+          const Item nx = decode_item<DEAL>(item_idx, a, n_pairs_q, n_kt);
+          const int n_it = f.half ? f.n_pairs / 8 : f.n_pairs / 4;
+          rotate_q_rows2<DQK>(q_smem(qa) + r * 128, q_smem(qb) + r * 128, r, a.q_offset + nx.qt0 * BM + r,
+                              a.rope_offset, f.n_pairs, f.half != 0, f_hi, f_lo, t * (n_it / 2),
+                              t ? n_it : n_it / 2);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(&bars->q_ready[qa]);
+        mbar_arrive(&bars->q_ready[qb]);
+      } else {
+        if (!warp_wait(&bars->q_full[qs], qp, wc)) return false;
+        if (f.n_pairs) {
+          const Item nx = decode_item<DEAL>(item_idx, a, n_pairs_q, n_kt);
+          rotate_q_row<DQK>(q_smem(qs) + r * 128, r, a.q_offset + (nx.qt0 + t * nx.dq) * BM + r, a.rope_offset,
+                            f.n_pairs, f.half != 0, f_hi, f_lo);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(&bars->q_ready[qs]);
       }
-      mbar_arrive(&bars->q_ready[qs]);
       return true;
     };
     int idx = item_at<DEAL>(0);
