@@ -57,6 +57,9 @@ CASES = [
     (2, 1024, 4, 4, 128, 1e4, True),   # eight tiles per head
     (1, 130, 2, 2, 96, 1e4, True),     # CUDA-core path (D_h 96)
     (1, 64, 2, 1, 256, 1e4, True),     # CUDA-core path (D_h 256)
+    (1, 384, 6, 2, 128, 1e4, True),    # GQA groups of 3: items of two adjacent Q tiles
+    (2, 640, 8, 4, 128, 5e5, True),    # GQA groups of 2 over a batch: items of one Q tile of two heads
+    (1, 333, 4, 2, 128, 1e4, False),   # GQA head-pair items without the mask, ragged tail
 ]
 
 
