@@ -22,15 +22,19 @@
 //               shuffles.  P is written back over S in TMEM as bf16.  The output
 //               is rescaled only when the row maximum grows by more than 2^8
 //               (exact: l and O always share the same reference maximum).
-//   A work item is two adjacent Q tiles of one (batch, head); while one
-//   warpgroup computes its softmax, the tensor core runs the other tile's MMAs.
-//   Items are taken heaviest-first (latest Q tiles see the most keys), dealt to the
-//   CTAs in waves that alternate direction.
-// RoPE: the query tile is rotated in shared memory right after its TMA load
-// (once per item, by the softmax warpgroup, with hardware sin/cos); keys arrive
-// already rotated (written once by the rope pass).  The Q tiles cycle through
-// three shared-memory slots, so the next item's first tile is in place before the
-// current item ends.
+//   A work item is two Q tiles that read the same K/V tiles: with GQA, one Q tile
+//   of two query heads of a K/V group (the tiles then see the same keys), else two
+//   adjacent Q tiles of one (batch, head); while one warpgroup computes its softmax,
+//   the tensor core runs the other tile's MMAs.  Items are taken heaviest-first
+//   (latest Q tiles see the most keys), dealt to the CTAs in waves that alternate
+//   direction.
+// RoPE: the query tiles are rotated in shared memory right after their TMA load
+// (once per item, with hardware sin/cos; for a GQA item both warpgroups rotate
+// both tiles, each angle serving the two heads); keys arrive already rotated
+// (written once by the rope pass).  The Q tiles cycle through three shared-memory
+// slots, so the next item's first tile is in place before the current item ends.
+// The epilogue exchanges each row's output among groups of four lanes, so that
+// every store instruction writes 64-byte row segments.
 // Head dims: (64, 64) and (128, 128); the MLA prefill shape (192, 128) runs on the
 // CTA-pair kernel of prefill_pair.cu.
 // TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1,
