@@ -77,11 +77,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(x);
 }
 
-// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
+// Exchange a 16-byte value with the lane whose index differs by the bits of mask.
 __device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask) {
   return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, mask), __shfl_xor_sync(0xffffffffu, v.y, mask),
                     __shfl_xor_sync(0xffffffffu, v.z, mask), __shfl_xor_sync(0xffffffffu, v.w, mask));
 }
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
