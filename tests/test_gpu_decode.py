@@ -272,6 +272,8 @@ TC_GQA = [
     (2, 64, 4, 260, 1e4),     # G = 16: the whole padded operand
     (2, 32, 8, 9000, 5e5),    # several 4096-key work units per sequence
     (5, 32, 8, 128, 5e5),     # exactly one tile
+    (128, 8, 2, 4097, 5e5),   # 256 (sequence, chunk) pairs: the most the kernel ranks longest first
+    (300, 8, 2, 700, 1e4),    # 300 pairs: claimed in sequence order
 ]
 
 
