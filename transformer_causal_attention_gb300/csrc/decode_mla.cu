@@ -47,9 +47,9 @@
 // their MMA.
 //
 // Keys of all sequences, laid end to end with a gap of kPieceGap virtual keys
-// between two sequences, are split evenly over the pairs (a pair's range may cross
-// sequence ends; the gap charges a pair that starts a new sequence for the new
-// query, its rotation and a pipeline refill); each (pair, sequence) piece writes
+// between two sequences, are split evenly over the pairs at whole rounds (a pair's
+// range may cross sequence ends; the gap charges a pair that starts a new sequence
+// for the new query, its rotation and a pipeline refill); each (pair, sequence) piece writes
 // one normalised partial, merged per sequence by mla_combine_kernel with the
 // log-sum-exp rule of the online softmax ("Transformer架构完全深度解析" §13).
 // Roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer (even
@@ -142,9 +142,15 @@ static_assert(sizeof(Bars) <= 512, "barrier block");
 constexpr long long kPieceGap = 1280;
 
 // Start of pair p in effective key positions (sequence b's key x sits at prefix[b] + gap b + x;
-// Teff = T + gap (B - 1)), and as the first real key at or after it.
+// Teff = T + gap (B - 1)), and as a real key: inside a sequence, the start is rounded down to a
+// whole round of keys, so that only a sequence's last round is partial (a round split between two
+// pairs would run its MMAs twice: at 32 x 32768 keys 4148 rounds instead of 4096, and 0.3517
+// against 0.3499 ms); in a gap, it is the next sequence's first key.
 __device__ __forceinline__ long long pair_start_eff(int p, long long Teff, int P) {
   return static_cast<long long>(p) * Teff / P;
+}
+__device__ __forceinline__ long long round_down_keys(long long o) {
+  return o & ~static_cast<long long>(kRoundKeys - 1);
 }
 __device__ __forceinline__ long long pair_start_key(int p, long long Teff, int P, const int* prefix, int nb) {
   const long long E = pair_start_eff(p, Teff, P);
@@ -154,7 +160,7 @@ __device__ __forceinline__ long long pair_start_key(int p, long long Teff, int P
     if (prefix[mid] + kPieceGap * mid <= E) lo = mid; else hi = mid - 1;
   }
   const long long o = E - (prefix[lo] + kPieceGap * lo);
-  return o < prefix[lo + 1] - prefix[lo] ? prefix[lo] + o : prefix[lo + 1];
+  return o < prefix[lo + 1] - prefix[lo] ? prefix[lo] + round_down_keys(o) : prefix[lo + 1];
 }
 
 // The keys of pair p as pieces, one per sequence it touches.
@@ -874,16 +880,22 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(DecodeA
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
   const long long Teff = total + kPieceGap * (a.B - 1);
-  const long long e0 = before + kPieceGap * b;                                // effective position of
-  const long long e1 = e0 + min(max(a.seqlens[b], 1), a.max_len) - 1;      // sequence b's first, last key
-  // pair holding effective position e: the largest p with floor(p Teff / P) <= e
+  const long long Lb = min(max(a.seqlens[b], 1), a.max_len);
+  const long long e0 = before + kPieceGap * b;  // effective position of
+  const long long e1 = e0 + Lb - 1;              // sequence b's first, last key
+  // pair holding effective position e: the largest p with floor(p Teff / P) <= e.  Rounding the
+  // starts down to whole rounds moves keys of b only between these pairs: no pair before p_lo
+  // starts inside b, and a pair after p_hi starts at or after b's end, where nothing is rounded.
   const int p_lo = static_cast<int>(((e0 + 1) * P - 1) / Teff);
   const int p_hi = static_cast<int>(((e1 + 1) * P - 1) / Teff);
   const int np = p_hi - p_lo + 1;
-  auto piece_lse = [&](int j) {  // -inf for a pair whose key range is empty (it wrote nothing)
-    // (a pair between the two holding e0 and e1 covers keys of sequence b only, so it is empty
-    // exactly when its effective range is)
-    if (pair_start_eff(p_lo + j + 1, Teff, P) <= pair_start_eff(p_lo + j, Teff, P)) return -INFINITY;
+  auto start_in_b = [&](int q) -> long long {  // pair q's first key as an offset into b, clamped to [0, Lb]
+    const long long E = pair_start_eff(q, Teff, P);
+    if (E <= e0) return 0;
+    return E - e0 < Lb ? round_down_keys(E - e0) : Lb;
+  };
+  auto piece_lse = [&](int j) {  // -inf for a pair that holds no key of b (it wrote nothing for b)
+    if (start_in_b(p_lo + j + 1) <= start_in_b(p_lo + j)) return -INFINITY;
     return a.ws_lse[(static_cast<long long>(p_lo + j) + b) * a.n_h + h];
   };
   float M = -INFINITY;
