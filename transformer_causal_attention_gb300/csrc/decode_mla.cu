@@ -144,8 +144,8 @@ constexpr long long kPieceGap = 1280;
 // Start of pair p in effective key positions (sequence b's key x sits at prefix[b] + gap b + x;
 // Teff = T + gap (B - 1)), and as a real key: inside a sequence, the start is rounded down to a
 // whole round of keys, so that only a sequence's last round is partial (a round split between two
-// pairs would run its MMAs twice: at 32 x 32768 keys 4148 rounds instead of 4096, and 0.3517
-// against 0.3499 ms); in a gap, it is the next sequence's first key.
+// pairs would run its MMAs twice: at 32 x 32768 keys over 76 pairs, 4130 rounds instead of 4096,
+// and 0.3517 against 0.3499 ms); in a gap, it is the next sequence's first key.
 __device__ __forceinline__ long long pair_start_eff(int p, long long Teff, int P) {
   return static_cast<long long>(p) * Teff / P;
 }
