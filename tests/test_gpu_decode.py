@@ -145,6 +145,8 @@ def test_mla_decode_batch_limit(lib, B):
     ([3, 1, 1], 0.0),
     ([257], 1e4),            # a second round holding a single valid key
     ([255, 1, 256], 0.0),
+    ([4000, 3999, 4001, 4000], 1e4),  # pair starts ~261 keys apart: rounded to whole rounds, some
+                                      # pairs hold two rounds and their neighbours none
 ])
 def test_mla_decode_few_keys(lib, lens, rope):
     # far fewer keys than CTA pairs x 256: most pairs get an empty key range, and the partials
