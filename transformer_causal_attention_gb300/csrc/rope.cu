@@ -93,6 +93,49 @@ __device__ __forceinline__ void rotate_chunk_rows(const T* src, T* dst, long lon
   }
 }
 
+// Rows whose chunks one thread loads before it stores any of them, so that its loads are in
+// flight together (a chunk is 16 bytes of bf16; kept as loaded until its row is rotated).
+constexpr int kRowBatch = 8;
+
+// bf16, adjacent pairs: the 8-dim chunk at src of n_rows rows stride elements apart, rotated by
+// the angles of pairs rel / 2 .. rel / 2 + 3 at position pos, to dst.  In place (dst == src) is
+// fine: each row is stored after its own load.
+__device__ __forceinline__ void rotate_rows_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst, long long stride,
+                                                 int n_rows, int rel, int pos, const SmemFreq& f) {
+  float sn[4], cs[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) rope_sincos(pos, f.hi[rel / 2 + p], f.lo[rel / 2 + p], &sn[p], &cs[p]);
+  for (int hb = 0; hb < n_rows; hb += kRowBatch) {
+    uint4 raw[kRowBatch];
+#pragma unroll
+    for (int e = 0; e < kRowBatch; ++e)
+      if (hb + e < n_rows) raw[e] = *reinterpret_cast<const uint4*>(src + (hb + e) * stride);
+#pragma unroll
+    for (int e = 0; e < kRowBatch; ++e)
+      if (hb + e < n_rows) {
+        float x[8];
+        bf16x8_to_f32(raw[e], x);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) rotate_pair(x[2 * p], x[2 * p + 1], sn[p], cs[p]);
+        *reinterpret_cast<uint4*>(dst + (hb + e) * stride) = f32_to_bf16x8(x);
+      }
+  }
+}
+
+// bf16: the 8-dim chunk at src of n_rows rows copied to dst as it is, loads batched as above.
+__device__ __forceinline__ void copy_rows_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst, long long stride,
+                                               int n_rows) {
+  for (int hb = 0; hb < n_rows; hb += kRowBatch) {
+    uint4 raw[kRowBatch];
+#pragma unroll
+    for (int e = 0; e < kRowBatch; ++e)
+      if (hb + e < n_rows) raw[e] = *reinterpret_cast<const uint4*>(src + (hb + e) * stride);
+#pragma unroll
+    for (int e = 0; e < kRowBatch; ++e)
+      if (hb + e < n_rows) *reinterpret_cast<uint4*>(dst + (hb + e) * stride) = raw[e];
+  }
+}
+
 template <typename T, int CH>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq rf) {
   __shared__ float freq[2 * kMaxRopePairs];
@@ -112,12 +155,22 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq rf) {
     if (rel >= 0 && rel < a.rope_dims) {
       if (f.half && rel >= f.n_pairs) continue;  // rotated by the owner of its partner chunk
       const int pos = a.positions ? a.positions[tok] : a.pos_offset + s;
+      if constexpr (sizeof(T) == 2 && CH == 8) {
+        if (!f.half) {
+          rotate_rows_bf16(in + off, out + off, a.D, a.n_heads, rel, pos, f);
+          continue;
+        }
+      }
       rotate_chunk_rows<T, CH>(in + off, out + off, a.D, a.n_heads, rel, pos, f);
     } else if (in != out) {
-      for (int h = 0; h < a.n_heads; ++h) {
-        float x[CH];
-        load_chunk<T, CH>(in + off + h * a.D, x);
-        store_chunk<T, CH>(out + off + h * a.D, x);
+      if constexpr (sizeof(T) == 2 && CH == 8) {
+        copy_rows_bf16(in + off, out + off, a.D, a.n_heads);
+      } else {
+        for (int h = 0; h < a.n_heads; ++h) {
+          float x[CH];
+          load_chunk<T, CH>(in + off + h * a.D, x);
+          store_chunk<T, CH>(out + off + h * a.D, x);
+        }
       }
     }
   }
@@ -125,13 +178,14 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, RopeFreq rf) {
 
 // One thread per (sequence b, new token c, 8-dim chunk): the new key row is
 // rotated at its absolute position start[b] + c and written to that cache
-// slot for every KV head, the value row is copied next to it.
-template <typename T>
+// slot for every KV head, the value row is copied next to it (bf16: the heads'
+// chunks in batches of kRowBatch loads before their stores).
 //
 // A decode step appends one token per sequence: too few (token, chunk) items to keep
 // the GPU's loads in flight when each thread walks all heads one after another, so the
 // launcher then gives every head its own thread (head_groups = n_kv; each thread computes
 // its own sin/cos), and otherwise one thread per (token, chunk) for all heads.
+template <typename T>
 __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq rf) {
   __shared__ float freq[2 * kMaxRopePairs];
   const SmemFreq f = stage_freq(rf, freq);
@@ -157,6 +211,12 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
       T* dst = static_cast<T*>(a.kcache) + (slot * a.n_kv + h0) * a.D_qk + d0;
       if (rel >= 0 && rel < 2 * f.n_pairs) {
         if (f.half && rel >= f.n_pairs) continue;  // written with its partner chunk
+        if constexpr (sizeof(T) == 2) {
+          if (!f.half) {
+            rotate_rows_bf16(src, dst, a.D_qk, hpt, rel, pos, f);
+            continue;
+          }
+        }
         rotate_chunk_rows<T, 8>(src, dst, a.D_qk, hpt, rel, pos, f);
       } else {
         for (int h = 0; h < hpt; ++h) {
@@ -170,10 +230,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a, RopeFreq
       const T* src = static_cast<const T*>(a.v_new) + (bc * a.n_kv + h0) * a.D_v + d0;
       T* dst = static_cast<T*>(a.vcache) + slot * a.v_token_stride + h0 * a.D_v + d0;
       if (a.v_token_stride % 8 == 0) {  // every value chunk starts on a 16-byte boundary: copy whole chunks
-        for (int h = 0; h < hpt; ++h) {
-          float x[8];
-          load_chunk<T, 8>(src + h * a.D_v, x);
-          store_chunk<T, 8>(dst + h * a.D_v, x);
+        if constexpr (sizeof(T) == 2) {  // 16-byte chunks as they are
+          copy_rows_bf16(src, dst, a.D_v, hpt);
+        } else {
+          for (int h = 0; h < hpt; ++h) {
+            float x[8];
+            load_chunk<T, 8>(src + h * a.D_v, x);
+            store_chunk<T, 8>(dst + h * a.D_v, x);
+          }
         }
       } else {
         for (int h = 0; h < hpt; ++h)
