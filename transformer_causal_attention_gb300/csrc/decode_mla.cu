@@ -137,9 +137,11 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Five rounds of keys: at 32 x 32768 a gap of 0 / 640 / 1280 / 2560 keys measured 0.363 / 0.358 /
-// 0.354 / 0.363 ms (a pair that starts a second sequence otherwise finishes last).
-constexpr long long kPieceGap = 1280;
+// Three rounds of keys (a pair that starts a second sequence otherwise finishes last): at
+// 32 x 32768, with the pair starts rounded to whole rounds, gaps of 256 / 512 / 768 / 1280 / 1792
+// keys measured 0.3526 / 0.3498 / 0.3470 / 0.3499 / 0.3531 ms (before the rounding, 0 / 640 /
+// 1280 / 2560 keys measured 0.363 / 0.358 / 0.354 / 0.363 ms).
+constexpr long long kPieceGap = 768;
 
 // Start of pair p in effective key positions (sequence b's key x sits at prefix[b] + gap b + x;
 // Teff = T + gap (B - 1)), and as a real key: inside a sequence, the start is rounded down to a
