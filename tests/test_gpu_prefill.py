@@ -60,6 +60,8 @@ CASES = [
     (1, 384, 6, 2, 128, 1e4, True),    # GQA groups of 3: items of two adjacent Q tiles
     (2, 640, 8, 4, 128, 5e5, True),    # GQA groups of 2 over a batch: items of one Q tile of two heads
     (1, 333, 4, 2, 128, 1e4, False),   # GQA head-pair items without the mask, ragged tail
+    (4, 1000, 24, 24, 64, 0.0, True),  # fewer than four items per CTA: dealt by a host-computed table
+    (3, 1100, 32, 32, 64, 1e4, True),  # the same with RoPE; the table leaves four CTAs without items
 ]
 
 

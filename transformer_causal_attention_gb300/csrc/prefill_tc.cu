@@ -41,7 +41,12 @@
 //               [256, 256+D_v) O of tile 0, [256+D_v, 256+2D_v) O of tile 1.
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
+#include <memory>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "kernels.h"
 
@@ -123,7 +128,7 @@ struct Item {
   __device__ __forceinline__ int load_at(int v) const { return v < ns_u ? v : r0.jl + v - ns_u; }
 };
 
-__device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, int n_kt) {
+__host__ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, int n_kt) {
   TileRange r;
   if (!a.causal) {
     r.ns = 0;
@@ -148,6 +153,16 @@ __device__ __forceinline__ TileRange tile_range(int qt, const PrefillArgs& a, in
 constexpr int kDealTiles = 0;      // two adjacent Q tiles of one (batch, head), heaviest-first waves
 constexpr int kDealTilesFold = 1;  // the same items, folded (below)
 constexpr int kDealHeads = 2;      // one Q tile of two heads of a K/V group, heaviest-first waves
+constexpr int kDealTable = 3;      // the items of kDealTiles, dealt by a table the host computes
+
+// The table of a small launch: CTA c takes items item[start[c]], ..., item[start[c + 1] - 1] (item
+// indices as kDealTiles numbers them).  It travels with the kernel's parameters.
+constexpr int kTableCtas = 256;
+constexpr int kTableItems = 1024;
+struct DealTable {
+  uint16_t start[kTableCtas + 1];
+  uint16_t item[kTableItems];
+};
 
 // Index of this CTA's k-th work item.  Items are sorted heaviest-first and dealt out in waves
 // of gridDim.x, every other wave in reverse CTA order, so that no CTA takes the heaviest item of
@@ -163,8 +178,12 @@ constexpr int kDealHeads = 2;      // one Q tile of two heads of a K/V group, he
 // The dealing is a template parameter: a run-time switch here cost the Llama-3-8B
 // prefill 2.7% (register spills in the item loops).
 template <int DEAL>
-__device__ __forceinline__ int item_at(uint32_t k) {
+__device__ __forceinline__ int item_at(const DealTable& tbl, int n_items, uint32_t k) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if constexpr (DEAL == kDealTable) {
+    const int j = tbl.start[c] + static_cast<int>(k);
+    return j < tbl.start[c + 1] ? tbl.item[j] : n_items;
+  }
   if constexpr (DEAL == kDealTilesFold) return 2 * (static_cast<int>(k >> 1) * g + c) + static_cast<int>(k & 1u);
   return static_cast<int>(k) * g + ((k & 1u) ? g - 1 - c : c);
 }
@@ -350,7 +369,7 @@ template <int DQK, int DV, int DEAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RopeFreq f,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ DealTable tbl) {
   using C = Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   // aligned by pointer arithmetic on the shared array, so that the compiler keeps shared-memory addressing
@@ -447,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued = 0, last_ph = 0;  // bit s: stage s had a load issued / its phase parity
         uint32_t q_armed = 0, q_last = 0, it = 0;  // bit q: slot q loaded / parity of its last load
         uint32_t qs = 0, qp = 0;                    // slot and parity of position 2 it + t
-        for (int idx = item_at<DEAL>(it); idx < n_items; idx = item_at<DEAL>(++it)) {
+        for (int idx = item_at<DEAL>(tbl, n_items, it); idx < n_items; idx = item_at<DEAL>(tbl, n_items, ++it)) {
           const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
           if (is_v) {
             for (int t = 0; t < 2; ++t, q_advance(qs, qp, 1)) {
@@ -518,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kOCol0 + t * DV, tmem + t * 128u + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int idx = item_at<DEAL>(it); idx < n_items; idx = item_at<DEAL>(++it)) {
+        for (int idx = item_at<DEAL>(tbl, n_items, it); idx < n_items; idx = item_at<DEAL>(tbl, n_items, ++it)) {
           const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
           bool q_seen0 = false, q_seen1 = false, pv_seen0 = false, pv_seen1 = false;
           uint32_t qs1 = qs0, qp1 = qp0;
@@ -678,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    int idx = item_at<DEAL>(0);
+    int idx = item_at<DEAL>(tbl, n_items, 0);
     if (idx < n_items && !prepare_q(cur_qs, cur_qp, idx)) idx = n_items;
     while (idx < n_items) {
       const Item itm = decode_item<DEAL>(idx, a, n_pairs_q, n_kt);
@@ -797,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->p_full[t]);
       }
       if (!ok) break;
-      const int next_idx = item_at<DEAL>(it + 1);
+      const int next_idx = item_at<DEAL>(tbl, n_items, it + 1);
       uint32_t nxt_qs = cur_qs, nxt_qp = cur_qp;
       q_advance(nxt_qs, nxt_qp, 2);
       if (next_idx < n_items && !prepare_q(nxt_qs, nxt_qp, next_idx)) break;
@@ -869,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 // Per instantiation, one bit per device that has been prepared.
-std::atomic<unsigned> g_ready[5];
+std::atomic<unsigned> g_ready[6];
 
 // Opt in to the kernel's shared memory and check, once per process and device,
 // that the compiled kernel holds enough registers per thread for its register
@@ -892,12 +911,98 @@ cudaError_t prepare(K kernel, int smem_bytes, std::atomic<unsigned>* ready) {
 
 template <int DQK, int DV, int DEAL = kDealTiles>
 cudaError_t launch(const PrefillArgs& a, const RopeFreq& rope, const CUtensorMap* maps, int grid, cudaStream_t st,
-                   std::atomic<unsigned>* ready) {
+                   std::atomic<unsigned>* ready, const DealTable& tbl) {
   auto k = prefill_tc_kernel<DQK, DV, DEAL>;
   const cudaError_t e = prepare(k, Cfg<DQK, DV>::kSmemBytes, ready);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, Cfg<DQK, DV>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2]);
+  k<<<grid, kThreads, Cfg<DQK, DV>::kSmemBytes, st>>>(a, rope, maps[0], maps[1], maps[2], tbl);
   return cudaGetLastError();
+}
+}  // namespace
+
+namespace {
+// Dealing table of a small launch (fewer than four items per CTA, where the items' sizes are few
+// and coarse and heaviest-first waves leave the busiest CTA well above the mean).  An item costs
+// its loaded key tiles at 17 units each (a turn of both Q tiles, ~1.7 us) plus 40 for its
+// boundary (~4 us).  First-fit decreasing packs the items into at most `grid` CTAs under a cap,
+// and a binary search takes the smallest cap that fits; the table is used only when that cap is
+// below the busiest CTA of the waves.  Tables are cached per launch shape.
+struct TableKey {
+  int B, n_h, S, S_k, q_offset, causal, window, n_sink, grid;
+  bool operator==(const TableKey& o) const {
+    return B == o.B && n_h == o.n_h && S == o.S && S_k == o.S_k && q_offset == o.q_offset && causal == o.causal &&
+           window == o.window && n_sink == o.n_sink && grid == o.grid;
+  }
+};
+
+bool build_table(const PrefillArgs& a, int n_items, int grid, DealTable* t) {
+  if (grid > kTableCtas || n_items > kTableItems || n_items >= 4 * grid) return false;
+  const int n_qt = (a.S + BM - 1) / BM, n_kt = (a.S_k + BN - 1) / BN;
+  const int n_pairs_q = (n_qt + 1) / 2, bh_count = a.B * a.n_h;
+  std::vector<int> w(n_items);
+  long long total = 0;
+  for (int idx = 0; idx < n_items; ++idx) {  // the kDealTiles numbering of decode_item
+    const int p = n_pairs_q - 1 - idx / bh_count;
+    const TileRange r0 = tile_range(2 * p, a, n_kt), r1 = tile_range(2 * p + 1, a, n_kt);
+    w[idx] = 17 * (r0.ns + r1.jh - r0.jl + 1) + 40;
+    total += w[idx];
+  }
+  // busiest CTA of the heaviest-first waves in alternating direction
+  std::vector<long long> load(grid, 0);
+  for (int idx = 0; idx < n_items; ++idx) {
+    const int k = idx / grid, j = idx % grid;
+    load[(k & 1) ? grid - 1 - j : j] += w[idx];
+  }
+  const long long waves_max = *std::max_element(load.begin(), load.end());
+  std::vector<int> order(n_items);
+  for (int i = 0; i < n_items; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return w[x] > w[y]; });
+  std::vector<int> bin(n_items);
+  auto ffd = [&](long long cap) {
+    int used = 0;
+    std::fill(load.begin(), load.end(), 0);
+    for (int i : order) {
+      int b = 0;
+      while (b < used && load[b] + w[i] > cap) ++b;
+      if (b == used) {
+        if (used == grid) return false;
+        ++used;
+      }
+      load[b] += w[i];
+      bin[i] = b;
+    }
+    return true;
+  };
+  long long lo = std::max<long long>(w[order[0]], (total + grid - 1) / grid), hi = waves_max - 1;
+  if (lo > hi || !ffd(hi)) return false;
+  while (lo < hi) {
+    const long long mid = (lo + hi) / 2;
+    if (ffd(mid)) hi = mid; else lo = mid + 1;
+  }
+  ffd(hi);
+  int pos = 0;
+  for (int c = 0; c < grid; ++c) {
+    t->start[c] = static_cast<uint16_t>(pos);
+    for (int i : order)  // heaviest first within a CTA
+      if (bin[i] == c) t->item[pos++] = static_cast<uint16_t>(i);
+  }
+  t->start[grid] = static_cast<uint16_t>(pos);
+  return true;
+}
+
+// The table for this launch, or nullptr (heaviest-first waves).
+const DealTable* deal_table(const PrefillArgs& a, int n_items, int grid) {
+  static std::mutex mu;
+  static std::vector<std::pair<TableKey, std::unique_ptr<DealTable>>> cache;  // nullptr: no table
+  const TableKey key{a.B, a.n_h, a.S, a.S_k, a.q_offset, a.causal, a.window, a.n_sink, grid};
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : cache)
+    if (e.first == key) return e.second.get();
+  std::unique_ptr<DealTable> t(new DealTable());
+  if (!build_table(a, n_items, grid, t.get())) t.reset();
+  if (cache.size() >= 64) cache.erase(cache.begin());
+  cache.emplace_back(key, std::move(t));
+  return cache.back().second.get();
 }
 }  // namespace
 
@@ -912,16 +1017,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const 
   const long long n_items =
       heads ? n_work_items<kDealHeads>(a.B, a.n_h, n_qt) : n_work_items<kDealTiles>(a.B, a.n_h, n_qt);
   const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
+  static const DealTable kNoTable{};
+  const DealTable* tbl = (!heads && !a.fold) ? deal_table(a, static_cast<int>(n_items), grid) : nullptr;
   cudaError_t e;
   // folded dealing is built for the two larger head dims (D = 64 prompts whose K/V
-  // pass twice the L2 take the plain dealing)
+  // pass twice the L2 take the plain dealing); the dealing table only for D = 64
   if (a.D == 64)
-    e = heads ? launch<64, 64, kDealHeads>(a, rope, maps, grid, st, &g_ready[3])
-              : launch<64, 64>(a, rope, maps, grid, st, &g_ready[0]);
+    e = heads ? launch<64, 64, kDealHeads>(a, rope, maps, grid, st, &g_ready[3], kNoTable)
+        : tbl ? launch<64, 64, kDealTable>(a, rope, maps, grid, st, &g_ready[5], *tbl)
+              : launch<64, 64>(a, rope, maps, grid, st, &g_ready[0], kNoTable);
   else if (a.D == 128)
-    e = a.fold ? launch<128, 128, kDealTilesFold>(a, rope, maps, grid, st, &g_ready[2])
-               : heads ? launch<128, 128, kDealHeads>(a, rope, maps, grid, st, &g_ready[4])
-                       : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1]);
+    e = a.fold ? launch<128, 128, kDealTilesFold>(a, rope, maps, grid, st, &g_ready[2], kNoTable)
+               : heads ? launch<128, 128, kDealHeads>(a, rope, maps, grid, st, &g_ready[4], kNoTable)
+                       : launch<128, 128>(a, rope, maps, grid, st, &g_ready[1], kNoTable);
   else
     e = cudaErrorInvalidValue;
   *launches += 1;
