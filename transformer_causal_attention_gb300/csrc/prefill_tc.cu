@@ -990,19 +990,31 @@ bool build_table(const PrefillArgs& a, int n_items, int grid, DealTable* t) {
   return true;
 }
 
-// The table for this launch, or nullptr (heaviest-first waves).
-const DealTable* deal_table(const PrefillArgs& a, int n_items, int grid) {
+// Copies the table for this launch into *out; false: heaviest-first waves.  (A copy, taken under
+// the lock: another thread may evict the cached entry before this launch is made.)
+bool deal_table(const PrefillArgs& a, int n_items, int grid, DealTable* out) {
   static std::mutex mu;
   static std::vector<std::pair<TableKey, std::unique_ptr<DealTable>>> cache;  // nullptr: no table
   const TableKey key{a.B, a.n_h, a.S, a.S_k, a.q_offset, a.causal, a.window, a.n_sink, grid};
   std::lock_guard<std::mutex> lock(mu);
+  const DealTable* t = nullptr;
+  bool found = false;
   for (const auto& e : cache)
-    if (e.first == key) return e.second.get();
-  std::unique_ptr<DealTable> t(new DealTable());
-  if (!build_table(a, n_items, grid, t.get())) t.reset();
-  if (cache.size() >= 64) cache.erase(cache.begin());
-  cache.emplace_back(key, std::move(t));
-  return cache.back().second.get();
+    if (e.first == key) {
+      t = e.second.get();
+      found = true;
+      break;
+    }
+  if (!found) {
+    std::unique_ptr<DealTable> nt(new DealTable());
+    if (!build_table(a, n_items, grid, nt.get())) nt.reset();
+    if (cache.size() >= 64) cache.erase(cache.begin());
+    cache.emplace_back(key, std::move(nt));
+    t = cache.back().second.get();
+  }
+  if (t == nullptr) return false;
+  *out = *t;
+  return true;
 }
 }  // namespace
 
@@ -1018,7 +1030,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const RopeFreq& rope, const 
       heads ? n_work_items<kDealHeads>(a.B, a.n_h, n_qt) : n_work_items<kDealTiles>(a.B, a.n_h, n_qt);
   const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
   static const DealTable kNoTable{};
-  const DealTable* tbl = (!heads && !a.fold) ? deal_table(a, static_cast<int>(n_items), grid) : nullptr;
+  DealTable table;
+  const DealTable* tbl = (!heads && !a.fold && deal_table(a, static_cast<int>(n_items), grid, &table)) ? &table
+                                                                                                     : nullptr;
   cudaError_t e;
   // folded dealing is built for the two larger head dims (D = 64 prompts whose K/V
   // pass twice the L2 take the plain dealing); the dealing table only for D = 64
